@@ -1,0 +1,60 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of ``oracle/oracle.c`` (on the CPU,
+in a temporary directory), builds it, and runs the oracle pin suites against
+the broken copy: at least one pin has to fail.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+MUTANTS = {
+    "drop_first_partial": ("acc = acc + orc_bf16_decode(partials[r][in_off + j]);",
+                           "acc = acc + (r ? orc_bf16_decode(partials[r][in_off + j]) : 0.0f);"),
+    "residual_sign": ("x[j] = x[j] + orc_bf16_decode(residual[in_off + j]);",
+                      "x[j] = x[j] - orc_bf16_decode(residual[in_off + j]);"),
+    "mean_over_h_minus_1": ("float variance = (float)(ss / (double)H);",
+                            "float variance = (float)(ss / (double)(H - 1));"),
+    "eps_dropped": ("float t = variance + eps;", "float t = variance;"),
+    "norm_of_rounded_x": ("float y = (x[j] * scale) * orc_bf16_decode(gamma[j]);",
+                          "float y = (orc_bf16_decode(orc_bf16_encode(x[j])) * scale) * orc_bf16_decode(gamma[j]);"),
+    "gamma_reversed": ("float y = (x[j] * scale) * orc_bf16_decode(gamma[j]);",
+                       "float y = (x[j] * scale) * orc_bf16_decode(gamma[H - 1 - j]);"),
+    "block_scale_240": ("float s = amax / 448.0f;", "float s = amax / 240.0f;"),
+    "fp4_nibbles_swapped": ("(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))"),
+    "e4m3_ties_away": ("r = nearbyint(a / q) * q;\n        if (r > 448.0)",
+                       "r = round(a / q) * q;\n        if (r > 448.0)"),
+    "e2m1_ties_away": ("r = nearbyint(a / q) * q;\n        if (r > 6.0)",
+                       "r = round(a / q) * q;\n        if (r > 6.0)"),
+    "bf16_truncates": ("double n = nearbyint(a / q);", "double n = floor(a / q);"),
+    "sf_over_4": ("orc_e4m3_encode(g_scale * (amax / 6.0f))", "orc_e4m3_encode(g_scale * (amax / 4.0f))"),
+    "qk_no_div_r": ("(double)(Vq / (float)R + eps)", "(double)(Vq + eps)"),
+    "qk_weight_slice": ("orc_bf16_decode(wq[r * Q + j])", "orc_bf16_decode(wq[j])"),
+    "qk_k_uses_q_mean": ("(double)(Vk / (float)R + eps)", "(double)(Vq / (float)R + eps)"),
+    "swizzle_rows_cols": ("return tile * 512 + j * 16 + i * 4 + (k % 4);",
+                          "return tile * 512 + i * 16 + j * 4 + (k % 4);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    import oracle
+
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mut = tmp_path / "oracle_mutant.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "liboracle_mutant.so"
+    oracle.build(force=True, src=str(mut), out=str(lib))
+    env = dict(os.environ, ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "tests/test_oracle_formats.py", "tests/test_oracle_fused.py",
+                        "tests/test_oracle_qk.py"], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 1, f"no pin caught mutant {name}:\n{r.stdout[-2000:]}"
