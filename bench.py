@@ -1,0 +1,529 @@
+"""Throughput of the fused reduce -> residual -> RMSNorm (+quant) path on GB300.
+
+One step = one ``ts_fused_reduce_norm(kARResidualRMSNorm)`` call over the
+R=8, T=4096, H=7168 bf16 workload (partials N(0, 0.5^2), residual N(0, 1),
+gamma U(0.5, 1.5), seed 0), inputs resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``value`` is tokens (rows) per second over all ranks (each rank runs the
+same per-GPU workload: weak scaling, no collective on the data path).  The
+line also carries the roofline of the kernel (algorithmic bytes / CUDA-event
+time against the measured HBM copy bandwidth), an end-to-end figure through
+the C ABI with host buffers and the copies in the timed region, the CPU
+oracle timed on a bounded sample of rows, the SM clocks sampled during the
+timed region, and ``rows``: the other patterns and workloads timed the same
+way (kAllReduce; FP8 per-tensor, FP8 1x128 blockwise, PartialOut on R=8,
+T=8192; NVFP4 on R=4, T=16384, H=5120 in both SF layouts; the sharded
+MiniMax QK-norm on R=8, T=32768; and the R=2, T=16 latency case).
+
+``--impl reference`` times the CPU oracle instead (host cores, bounded samples
+of the same workload per step); under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused reduce+RMSNorm(+quant) tokens/s and achieved HBM GB/s vs 8 TB/s, 1×GB300"
+WORKLOAD = ("kARResidualRMSNorm R=8 T=4096 H=7168: bf16 partials ~N(0,0.5^2), residual ~N(0,1), "
+            "gamma ~U(0.5,1.5), eps 1e-6, seed 0")
+EPS = 1e-6
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 10 ** 6
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (reads of R partials + residual, gamma once, all outputs)
+# ---------------------------------------------------------------------------
+
+def fused_bytes(pattern: int, R: int, T: int, H: int, P: int = 0, swizzled: bool = False,
+                allreduce_out: bool = False) -> int:
+    p = int(pattern)
+    rb = T * R * H * 2
+    wb = 0
+    if p == 0 or allreduce_out:
+        wb += T * H * 2
+    if p != 0:
+        rb += T * H * 2 + H * 2  # residual, gamma
+        wb += T * H * 2          # residual_out
+    if 2 <= p <= 5:
+        rb += 4                  # scale_factor
+    if p in (1, 4, 5):
+        wb += T * H * 2          # norm_out
+    if p in (7, 8):
+        wb += T * P * 2          # partial_norm_out
+    if p in (2, 4, 6, 7):
+        wb += T * H              # e4m3 codes
+    if p in (6, 7):
+        wb += T * (H // 128) * 4
+    if p in (3, 5):
+        wb += T * H // 2
+        wb += ((T + 127) // 128 * 128) * ((H // 16 + 3) // 4 * 4) if swizzled else T * (H // 16)
+    return rb + wb
+
+
+def qk_bytes(R: int, T: int, Q: int, K: int) -> int:
+    return T * R * (Q + K) * 2 * 2 + R * (Q + K) * 2
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def read_peaks() -> tuple[float, str]:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "reduce_residual_rmsnorm_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(key: str):
+    """dram read+write bytes per launch from the committed ncu summary, if it was
+    taken on the kernels as they are now (same source hash); else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    v = rec.get("bytes_per_launch", {}).get(key)
+    return None if v is None else int(v)
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 20):
+        self.index, self.period_ms, self.proc = index, period_ms, None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)  # let the first sample land
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest ``value`` over all ranks (every rank gets it)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reported baseline, never a target)
+# ---------------------------------------------------------------------------
+
+def oracle_rows_per_second(inp_host: dict, seconds: float, pattern: int = 1):
+    import numpy as np
+
+    import oracle
+    from reduce_residual_rmsnorm_gb300 import workloads as wl
+
+    parts = [wl.bits(p) for p in inp_host["partials"]]
+    res, gamma = wl.bits(inp_host["residual"]), wl.bits(inp_host["gamma"])
+    T = res.shape[0]
+    done, start, row = 0, time.perf_counter(), 0
+    chunk = 8
+    while True:
+        rows = (np.arange(chunk) + row) % T
+        oracle.fused_reduce_norm(pattern, parts, res, gamma, EPS, rows=rows)
+        done += chunk
+        row = (row + chunk) % T
+        el = time.perf_counter() - start
+        if el >= seconds:
+            return done / el, done, el
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the oracle on host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from reduce_residual_rmsnorm_gb300 import workloads as wl
+
+    shape = wl.WORKLOADS["C2"]
+    inp = wl.fused_inputs(shape, seed=0)
+    parts = [wl.bits(p) for p in inp["partials"]]
+    res, gamma = wl.bits(inp["residual"]), wl.bits(inp["gamma"])
+    t0 = time.perf_counter()
+    oracle.fused_reduce_norm(1, parts, res, gamma, EPS, rows=np.arange(4))
+    per_row = (time.perf_counter() - t0) / 4
+    budget = 120.0  # seconds for warm-up + timed steps together
+    rows_per_step = int(max(1, min(shape.T, budget / max(1, args.steps + args.warmup) / per_row)))
+    step_rows = lambda i: (np.arange(rows_per_step) + i * rows_per_step) % shape.T  # noqa: E731
+    for i in range(args.warmup):
+        oracle.fused_reduce_norm(1, parts, res, gamma, EPS, rows=step_rows(i))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.fused_reduce_norm(1, parts, res, gamma, EPS, rows=step_rows(args.warmup + i))
+    el = time.perf_counter() - t0
+    value = rows_per_step * args.steps / el
+    sample = (f"{rows_per_step} of the {shape.T} rows per step (pattern 1, R=8, H=7168), "
+              f"single-threaded C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "pattern": 1, "R": 8, "T": 4096, "H": 7168},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def time_launches(fn, iters: int, stream, warmup: int = 3) -> float:
+    """Average ms per call of ``fn`` (launching on ``stream``), CUDA events."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(iters):
+        fn()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def roofline_entry(nbytes: int, ms: float, peak: float) -> dict:
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"us": ms * 1e3, "bytes": nbytes, "gbs": gbs, "frac": gbs / peak}
+
+
+def measure_rows(dev, stream, peak: float, iters: int) -> dict:
+    import torch
+
+    import reduce_residual_rmsnorm_gb300 as pkg
+    from reduce_residual_rmsnorm_gb300 import workloads as wl
+
+    rows = {}
+    with torch.cuda.stream(stream):
+        # kAllReduce on the R=8, T=4096, H=7168 inputs
+        shape = wl.WORKLOADS["C2"]
+        inp = wl.fused_inputs(shape, seed=0, device=dev)
+        out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
+        ms = time_launches(lambda: pkg.ts_fused_reduce_norm(0, inp["partials"], allreduce_out=out,
+                                                            stream=stream), iters, stream)
+        rows["kAllReduce R=8 T=4096 H=7168"] = roofline_entry(fused_bytes(0, 8, 4096, 7168), ms, peak)
+        del inp, out
+
+        # FP8 per-tensor / blockwise / PartialOut on R=8, T=8192, H=7168 with outliers
+        shape = wl.WORKLOADS["C3"]
+        inp = wl.fused_inputs(shape, seed=0, device=dev)
+        T, H = shape.T, shape.H
+        res_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        norm = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS, residual_out=res_out,
+                                 norm_out=norm, stream=stream)
+        sigma = (448.0 / norm.float().abs().max()).reshape(1).to(torch.float32)
+        q8 = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        sc = torch.empty((T, H // 128), dtype=torch.float32, device=dev)
+        part = torch.empty((T, 1024), dtype=torch.bfloat16, device=dev)
+        cases = {
+            "kARResidualRMSNormFP8Quant R=8 T=8192 H=7168": (
+                2, dict(quant_out=q8), sigma, fused_bytes(2, 8, T, H)),
+            "kARResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168": (
+                6, dict(quant_out=q8, scale_out=sc), None, fused_bytes(6, 8, T, H)),
+            "kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024": (
+                7, dict(quant_out=q8, scale_out=sc, partial_norm_out=part), None, fused_bytes(7, 8, T, H, 1024)),
+            "kARResidualRMSNormPartialOut R=8 T=8192 H=7168 P=1024": (
+                8, dict(partial_norm_out=part), None, fused_bytes(8, 8, T, H, 1024)),
+        }
+        for name, (p, outs, sf, nb) in cases.items():
+            ms = time_launches(lambda: pkg.ts_fused_reduce_norm(p, inp["partials"], inp["residual"], inp["gamma"],
+                                                                EPS, sf, residual_out=res_out, stream=stream,
+                                                                **outs), iters, stream)
+            rows[name] = roofline_entry(nb, ms, peak)
+        del inp, res_out, norm, q8, sc, part
+
+        # NVFP4 on R=4, T=16384, H=5120, LINEAR and SWIZZLED_128x4
+        shape = wl.WORKLOADS["C4"]
+        inp = wl.fused_inputs(shape, seed=0, device=dev)
+        T, H = shape.T, shape.H
+        res_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        norm = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS, residual_out=res_out,
+                                 norm_out=norm, stream=stream)
+        g = (2688.0 / norm.float().abs().max()).reshape(1).to(torch.float32)
+        q4 = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
+        for layout, swz in ((pkg.SFLayout.LINEAR, False), (pkg.SFLayout.SWIZZLED_128x4, True)):
+            sf = torch.empty(pkg.sf_swizzled_shape(T, H) if swz else (T, H // 16), dtype=torch.uint8, device=dev)
+            ms = time_launches(lambda: pkg.ts_fused_reduce_norm(3, inp["partials"], inp["residual"], inp["gamma"],
+                                                                EPS, g, residual_out=res_out, quant_out=q4,
+                                                                scale_out=sf, sf_layout=layout, stream=stream),
+                               iters, stream)
+            rows[f"kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF {layout.name}"] = roofline_entry(
+                fused_bytes(3, 4, T, H, swizzled=swz), ms, peak)
+        del inp, res_out, norm, q4, sf
+
+        # MiniMax sharded QK-norm, R=8, T=32768, q 1024 | k 128 | v 128
+        qs = wl.WORKLOADS["C5"]
+        qi = wl.qk_inputs(qs, seed=0, device=dev)
+        qo = torch.empty((qs.T, qs.R * qs.q_shard), dtype=torch.bfloat16, device=dev)
+        ko = torch.empty((qs.T, qs.R * qs.k_shard), dtype=torch.bfloat16, device=dev)
+        ms = time_launches(lambda: pkg.ts_qk_norm_sharded(qi["shards"], qs.q_shard, qs.k_shard, qi["q_weight"],
+                                                          qi["k_weight"], EPS, qo, ko, stream=stream), iters, stream)
+        rows["MiniMax QK-RMSNorm R=8 T=32768 Q=1024 K=128"] = roofline_entry(
+            qk_bytes(qs.R, qs.T, qs.q_shard, qs.k_shard), ms, peak)
+        del qi, qo, ko
+
+        # latency case: R=2, T=16, H=4096 (L2-resident; reported in us)
+        shape = wl.WORKLOADS["C1"]
+        inp = wl.fused_inputs(shape, seed=0, device=dev)
+        ro = torch.empty((16, 4096), dtype=torch.bfloat16, device=dev)
+        no = torch.empty((16, 4096), dtype=torch.bfloat16, device=dev)
+        call = lambda: pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS,  # noqa
+                                                residual_out=ro, norm_out=no, stream=stream)
+        ms_stream = time_launches(call, max(iters, 200), stream)
+        graph = torch.cuda.CUDAGraph()
+        call()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(100):
+                call()
+        ms_graph = time_launches(graph.replay, 20, stream) / 100
+        rows["kARResidualRMSNorm R=2 T=16 H=4096 (latency)"] = {
+            "us_stream_launch": ms_stream * 1e3, "us_in_cuda_graph": ms_graph * 1e3,
+            "bytes": fused_bytes(1, 2, 16, 4096)}
+        del inp, ro, no, graph
+    torch.cuda.synchronize()
+    return rows
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import reduce_residual_rmsnorm_gb300 as pkg
+    from reduce_residual_rmsnorm_gb300 import workloads as wl
+
+    peak, peak_kind = read_peaks()
+    shape = wl.WORKLOADS["C2"]
+    R, T, H = shape.R, shape.T, shape.H
+    host_inp = wl.fused_inputs(shape, seed=0)
+    parts = host_inp["partials"].to(dev)
+    res = host_inp["residual"].to(dev)
+    gamma = host_inp["gamma"].to(dev)
+    res_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    norm_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    nbytes = fused_bytes(1, R, T, H)
+
+    def step():
+        pkg.ts_fused_reduce_norm(1, parts, res, gamma, EPS, residual_out=res_out, norm_out=norm_out,
+                                 stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    with sampler:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(ms_local, world, dev)
+    value = world * T / (ms * 1e-3)
+    achieved = nbytes / (ms_local * 1e-3) / 1e9
+
+    # end to end through the C ABI: pinned host inputs -> device, call, outputs -> host
+    h_parts = host_inp["partials"].pin_memory()
+    h_res = host_inp["residual"].pin_memory()
+    h_out_res = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    h_out_norm = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    d_parts = torch.empty_like(parts)
+    d_res = torch.empty_like(res)
+
+    def e2e_step():
+        d_parts.copy_(h_parts, non_blocking=True)
+        d_res.copy_(h_res, non_blocking=True)
+        pkg.ts_fused_reduce_norm(1, d_parts, d_res, gamma, EPS, residual_out=res_out, norm_out=norm_out,
+                                 stream=stream)
+        h_out_res.copy_(res_out, non_blocking=True)
+        h_out_norm.copy_(norm_out, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    with torch.cuda.stream(stream):
+        e2e_ms = time_launches(e2e_step, e2e_steps, stream, warmup=2)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    h2d = (h_parts.numel() + h_res.numel()) * 2
+    d2h = (h_out_res.numel() + h_out_norm.numel()) * 2
+    del h_parts, h_res, h_out_res, h_out_norm, d_parts, d_res
+
+    rows = None
+    if not args.no_rows:
+        rows = measure_rows(dev, stream, peak, args.row_iters)
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        rps, done, el = oracle_rows_per_second(host_inp, args.cpu_seconds)
+        cpu = {"value": rps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{done} rows of the R=8 T=4096 H=7168 kARResidualRMSNorm workload "
+                         f"(8-row batches, wrapping), {el:.1f} s of single-threaded C"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "pattern": 1, "R": R, "T": T, "H": H,
+                       "bytes_per_step": nbytes,
+                       "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB per step > 129 MB); no flush",
+                       "parallelism": f"replicas x{world} (rows are independent; no collective)"},
+            "achieved_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                         "traffic": recorded_traffic("fused_rows_kernel pattern 1 R=8 T=4096 H=7168")},
+            "e2e": {"value": T * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "cpu_baseline": cpu,
+            "gpu_launches": args.steps,
+            "clocks": sampler.summary(),
+            "kernel_source_hash": kernel_source_hash(),
+            "rows": rows,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="skip the other patterns/workloads")
+    ap.add_argument("--row-iters", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+/*
+ * ts_fused_norm.h: C ABI of the GB300 (sm_103a) fused "reduce R partials ->
+ * add residual -> RMSNorm -> optional FP8 / NVFP4 quantise" epilogue and of
+ * the tensor-parallel MiniMax QK-RMSNorm, restated for one GPU.
+ *
+ * What the calls compute is defined by three pages:
+ *   - tokenspeed `thirdparty/cuda/trtllm.py`: the `AllReduceFusionPattern`
+ *     codes (kept here with the same numbers), `QuantizationSFLayout`, and
+ *     `trtllm_allreduce_fusion` (its inputs, its optional outputs
+ *     allreduce_out / residual_out / norm_out / partial_norm_out /
+ *     quant_out / scale_out, rms_gamma, rms_eps, scale_factor, layout_code).
+ *   - tokenspeed `ops/communication/triton.py`: `amd_all_reduce_kernel` and
+ *     `amd_allreduce_residual_rmsnorm_kernel`, the executable statement of the
+ *     math (fp32 sum over peers in ascending order, + residual, mean of
+ *     squares, rsqrt(var + eps), x * scale * weight).
+ *   - vLLM `minimax_rms_norm/rms_norm_tp`: `_minimax_qk_norm_tp_eager`,
+ *     `_minimax_qk_var_kernel`, `_minimax_rms_apply_kernel`.
+ * On one GPU the R rank partials (or the R tensor-parallel shards) are R
+ * buffers in this GPU's memory: there is no communication, no workspace and
+ * no inter-GPU synchronisation.
+ *
+ * Conventions for every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *     library allocates nothing, keeps no state between calls and never
+ *     synchronises: a call validates its arguments on the host, enqueues one
+ *     kernel on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *     and returns.  Arrays of pointers (`partials`, `qkv_shards`) and the
+ *     `ts_outs_t` struct live in HOST memory and are read during the call only.
+ *   - bf16 tensors are row-major and contiguous unless a leading dimension is
+ *     given.  Tensor base pointers must be 16-byte aligned (128-bit vector
+ *     access); fp32 scalars / scale arrays need 4-byte alignment.
+ *   - Errors: the return value is TS_OK (0) or a negative ts_status_t.  All
+ *     argument checks run on the host before anything is launched, so a
+ *     rejected call touches no memory.  ts_last_error_detail() returns a
+ *     human-readable reason for the last failure on the calling thread.
+ *     TS_ERR_LAUNCH reports a CUDA error raised by the launch itself
+ *     (the CUDA error name is in the detail string).
+ */
+#ifndef TS_FUSED_NORM_H
+#define TS_FUSED_NORM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TS_API __attribute__((visibility("default")))
+#else
+#define TS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TS_OK = 0,
+    TS_ERR_BAD_PATTERN = -1, /* pattern code outside 0..8, or an unknown SF layout       */
+    TS_ERR_NULL = -2,        /* a required pointer is NULL                              */
+    TS_ERR_SHAPE = -3,       /* sizes out of range / not multiples the pattern requires  */
+    TS_ERR_ALIGN = -4,       /* a pointer is not aligned as required                     */
+    TS_ERR_UNSUPPORTED = -5, /* valid request this build does not implement, or an output
+                                pointer the pattern does not define                      */
+    TS_ERR_ALIAS = -6,       /* overlapping buffers (other than the allowed in-place ones) */
+    TS_ERR_LAUNCH = -7       /* the CUDA launch failed                                    */
+} ts_status_t;
+
+/* Codes identical to `AllReduceFusionPattern` (tokenspeed trtllm.py). */
+typedef enum {
+    TS_AR = 0,                                 /* kAllReduce                                  */
+    TS_AR_RES_RMS = 1,                         /* kARResidualRMSNorm                          */
+    TS_AR_RES_RMS_FP8 = 2,                     /* kARResidualRMSNormFP8Quant                  */
+    TS_AR_RES_RMS_FP4 = 3,                     /* kARResidualRMSNormFP4Quant                  */
+    TS_AR_RES_RMS_OUT_FP8 = 4,                 /* kARResidualRMSNormOutFP8Quant               */
+    TS_AR_RES_RMS_OUT_FP4 = 5,                 /* kARResidualRMSNormOutFP4Quant               */
+    TS_AR_RES_RMS_FP8_BLOCKWISE = 6,           /* kARResidualRMSNormFP8BlockWiseQuant         */
+    TS_AR_RES_RMS_PARTIAL_OUT_FP8_BLOCKWISE = 7, /* kARResidualRMSNormPartialOutFP8BlockWiseQuant */
+    TS_AR_RES_RMS_PARTIAL_OUT = 8              /* kARResidualRMSNormPartialOut                */
+} ts_pattern_t;
+
+/* Codes identical to `QuantizationSFLayout` (tokenspeed trtllm.py). */
+typedef enum {
+    TS_SF_SWIZZLED_128x4 = 0,
+    TS_SF_SWIZZLED_8x4 = 1, /* not implemented: TS_ERR_UNSUPPORTED */
+    TS_SF_LINEAR = 2
+} ts_sf_layout_t;
+
+/*
+ * Output set of ts_fused_reduce_norm.  Which members a pattern writes
+ * (R = required, o = optional: written when non-NULL, - = must be NULL):
+ *
+ *   pattern            allreduce_out residual_out norm_out partial_norm_out quant_out scale_out
+ *   0 kAllReduce             R            -          -           -             -         -
+ *   1 ResidualRMSNorm        o            R          R           -             -         -
+ *   2 ...FP8Quant            o            R          -           -             R         -
+ *   3 ...FP4Quant            o            R          -           -             R         R
+ *   4 ...OutFP8Quant         o            R          R           -             R         -
+ *   5 ...OutFP4Quant         o            R          R           -             R         R
+ *   6 ...FP8BlockWise        o            R          -           -             R         R
+ *   7 ...PartialOutFP8BW     o            R          -           R             R         R
+ *   8 ...PartialOut          o            R          o           R             -         -
+ *
+ *   allreduce_out     bf16 [T, H]: bf16(sum of partials).  May equal partials[0]
+ *                     (in place, as the Triton all_reduce writes its result
+ *                     into its input); no other overlap.
+ *   residual_out      bf16 [T, H]: bf16(sum + residual).  May equal `residual`.
+ *   norm_out          bf16 [T, H]: n = bf16((x * rsqrt(mean(x^2) + eps)) * gamma),
+ *                     x the unrounded fp32 sum + residual.
+ *   partial_norm_out  bf16 [T, partial_cols]: the first partial_cols columns of n
+ *                     (row stride partial_cols); the RMS still spans all H.
+ *   partial_cols      0 < P <= H, P % 8 == 0 (patterns 7, 8; ignored otherwise).
+ *   quant_out         patterns 2, 4, 6, 7: FP8 E4M3 codes, uint8 [T, H].
+ *                     patterns 3, 5: NVFP4 E2M1 codes, uint8 [T, H/2], two per
+ *                     byte, element 2k in the low nibble of byte k.
+ *   scale_out         patterns 6, 7: fp32 [T, H/128], s = amax(|n| over 128
+ *                     columns) / 448, codes e4m3(n / s) (0 for an all-zero group).
+ *                     patterns 3, 5: E4M3 scale factors, one per 16 columns,
+ *                     SF = e4m3(g * amax/6), codes e2m1(n * (g / value(SF))),
+ *                     laid out per sf_layout:
+ *                       TS_SF_LINEAR: uint8 [T, H/16];
+ *                       TS_SF_SWIZZLED_128x4: uint8 [ceil(T/128)*128,
+ *                       ceil(H/64)*4] in 512-byte tiles of 128 rows x 4
+ *                       columns; SF (m, k) at byte
+ *                       ((m/128)*(Kp/4) + k/4)*512 + (m%32)*16 + ((m%128)/32)*4 + k%4
+ *                       with Kp = ceil(H/64)*4.  Padding bytes are written as 0.
+ *   sf_layout         ts_sf_layout_t (patterns 3, 5; ignored otherwise).
+ */
+typedef struct {
+    void *allreduce_out;
+    void *residual_out;
+    void *norm_out;
+    void *partial_norm_out;
+    int64_t partial_cols;
+    void *quant_out;
+    void *scale_out;
+    int32_t sf_layout;
+    int32_t reserved; /* must be 0 */
+} ts_outs_t;
+
+/*
+ * ts_fused_reduce_norm: one AllReduceFusionPattern over T rows of width H
+ * (tokenspeed trtllm.py `trtllm_allreduce_fusion`; the math of tokenspeed
+ * triton.py `amd_allreduce_residual_rmsnorm_kernel` / `amd_all_reduce_kernel`):
+ *
+ *   a[t,j]  = ((0 + p0[t,j]) + p1[t,j]) + ... + p_{R-1}[t,j]      fp32, r ascending
+ *   x[t,j]  = a[t,j] + residual[t,j]                             fp32
+ *   s[t]    = rsqrt(sum_j x[t,j]^2 / H + eps)                    fp32
+ *   n[t,j]  = bf16((x[t,j] * s[t]) * gamma[j])
+ *   then the outputs listed above for the pattern.
+ *
+ *   pattern       ts_pattern_t.
+ *   partials      host array of R device pointers, each bf16 [T, H].
+ *   R             1..16.
+ *   residual      bf16 [T, H]; required for patterns 1..8 (ignored for 0).
+ *   gamma         bf16 [H] (rms_gamma); required for patterns 1..8.
+ *   eps           rms_eps, added inside the rsqrt (e.g. 1e-6).
+ *   scale_factor  device fp32[1]: the per-tensor FP8 scale sigma (patterns 2, 4:
+ *                 code = e4m3(n * sigma)) or the NVFP4 global scale g (patterns
+ *                 3, 5); required for 2..5, ignored otherwise.  A device pointer
+ *                 so the call can be captured in a CUDA graph.
+ *   T             rows (tokens), >= 0.  T == 0 validates and returns TS_OK.
+ *   H             hidden size: multiple of 8, <= 16384; multiple of 128 for
+ *                 patterns 6, 7; multiple of 16 for patterns 3, 5.
+ *   outs          host pointer to the output set (see ts_outs_t).
+ *   stream        cudaStream_t.
+ */
+TS_API int ts_fused_reduce_norm(int pattern, const void *const *partials, int R, const void *residual,
+                         const void *gamma, float eps, const float *scale_factor, int64_t T,
+                         int64_t H, const ts_outs_t *outs, void *stream);
+
+/*
+ * ts_qk_norm_sharded: MiniMax tensor-parallel QK-RMSNorm with the R shards
+ * resident on this GPU (vLLM rms_norm_tp `_minimax_qk_norm_tp_eager`, split
+ * as `_minimax_qk_var_kernel` + all-reduce of the [T, 2] fp32 variance +
+ * `_minimax_rms_apply_kernel`; here one fused kernel):
+ *
+ *   vq_r[t] = sum_{j<Q} x_r[t,j]^2 / Q,   vk_r[t] = sum_{j<K} x_r[t,Q+j]^2 / K   fp32
+ *   Vq[t]   = sum over r ascending of vq_r[t]   (likewise Vk)                fp32
+ *   q_out[t, r*Q + j] = bf16((x_r[t,j]   * rsqrt(Vq[t]/R + eps)) * q_weight[r*Q + j])
+ *   k_out[t, r*K + j] = bf16((x_r[t,Q+j] * rsqrt(Vk[t]/R + eps)) * k_weight[r*K + j])
+ *
+ *   qkv_shards    host array of R device pointers; shard r is bf16 [T, row_stride]
+ *                 holding q (Q columns) | k (K columns) | v (not read).
+ *   R             1..16.
+ *   T             tokens, >= 0 (T == 0 returns TS_OK).
+ *   row_stride    elements between consecutive tokens of a shard; multiple of 8,
+ *                 >= Q + K.
+ *   q_shard (Q)   8 <= Q <= 4096, multiple of 8.   k_shard (K): 8 <= K <= 1024,
+ *                 multiple of 8.
+ *   q_weight      bf16 [R*Q]; shard r uses q_weight[r*Q .. r*Q+Q).
+ *   k_weight      bf16 [R*K].
+ *   eps           added inside the rsqrt after the division by R.
+ *   q_out, ldq    bf16 [T, ldq], ldq >= R*Q, multiple of 8: shard r's block at
+ *                 columns r*Q .. r*Q+Q (the unsharded, hidden-concatenated layout).
+ *   k_out, ldk    bf16 [T, ldk], ldk >= R*K, multiple of 8.
+ *   Outputs must not overlap the shards, the weights or each other.
+ */
+TS_API int ts_qk_norm_sharded(const void *const *qkv_shards, int R, int64_t T, int64_t row_stride,
+                       int64_t q_shard, int64_t k_shard, const void *q_weight,
+                       const void *k_weight, float eps, void *q_out, int64_t ldq, void *k_out,
+                       int64_t ldk, void *stream);
+
+/* Static text for a ts_status_t value ("TS_OK", "TS_ERR_SHAPE", ...). */
+TS_API const char *ts_status_string(int status);
+
+/* Reason for the most recent failed call on the calling thread ("" if none).
+ * The string stays valid until the next call on the same thread. */
+TS_API const char *ts_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TS_FUSED_NORM_H */

@@ -1,0 +1,243 @@
+"""ctypes binding of ``libts_fused_norm.so`` (include/ts_fused_norm.h).
+
+Argument marshalling only: tensors become device pointers, the stream is
+PyTorch's current stream, and a non-zero status becomes a ``TsError``.  Every
+step of the computation runs in the library's CUDA kernels; there is no
+Python or CPU fallback, and calling without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+from typing import Sequence
+
+import torch
+
+from .build import LIB_PATH
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Pattern(enum.IntEnum):
+    """`AllReduceFusionPattern` codes (tokenspeed trtllm.py)."""
+    kAllReduce = 0
+    kARResidualRMSNorm = 1
+    kARResidualRMSNormFP8Quant = 2
+    kARResidualRMSNormFP4Quant = 3
+    kARResidualRMSNormOutFP8Quant = 4
+    kARResidualRMSNormOutFP4Quant = 5
+    kARResidualRMSNormFP8BlockWiseQuant = 6
+    kARResidualRMSNormPartialOutFP8BlockWiseQuant = 7
+    kARResidualRMSNormPartialOut = 8
+
+
+class SFLayout(enum.IntEnum):
+    """`QuantizationSFLayout` codes (tokenspeed trtllm.py)."""
+    SWIZZLED_128x4 = 0
+    SWIZZLED_8x4 = 1
+    LINEAR = 2
+
+
+class TsError(RuntimeError):
+    def __init__(self, status: int, name: str, detail: str):
+        super().__init__(f"{name}: {detail}")
+        self.status = status
+        self.name = name
+        self.detail = detail
+
+
+class TsOuts(ctypes.Structure):
+    _fields_ = [
+        ("allreduce_out", ctypes.c_void_p),
+        ("residual_out", ctypes.c_void_p),
+        ("norm_out", ctypes.c_void_p),
+        ("partial_norm_out", ctypes.c_void_p),
+        ("partial_cols", ctypes.c_int64),
+        ("quant_out", ctypes.c_void_p),
+        ("scale_out", ctypes.c_void_p),
+        ("sf_layout", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+EXPORTS = ("ts_fused_reduce_norm", "ts_qk_norm_sharded", "ts_status_string", "ts_last_error_detail")
+
+
+def library(path: str | None = None):
+    """Load the CUDA library (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build the CUDA library first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(p)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        lib.ts_fused_reduce_norm.argtypes = [ctypes.c_int, ctypes.POINTER(vp), ctypes.c_int, vp, vp,
+                                             ctypes.c_float, vp, i64, i64, ctypes.POINTER(TsOuts), vp]
+        lib.ts_fused_reduce_norm.restype = ctypes.c_int
+        lib.ts_qk_norm_sharded.argtypes = [ctypes.POINTER(vp), ctypes.c_int, i64, i64, i64, i64, vp, vp,
+                                           ctypes.c_float, vp, i64, vp, i64, vp]
+        lib.ts_qk_norm_sharded.restype = ctypes.c_int
+        lib.ts_status_string.argtypes = [ctypes.c_int]
+        lib.ts_status_string.restype = ctypes.c_char_p
+        lib.ts_last_error_detail.argtypes = []
+        lib.ts_last_error_detail.restype = ctypes.c_char_p
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        lib = library()
+        raise TsError(status, lib.ts_status_string(status).decode(),
+                      lib.ts_last_error_detail().decode())
+
+
+def ts_status_string(status: int) -> str:
+    return library().ts_status_string(int(status)).decode()
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _rows(ts: torch.Tensor | Sequence[torch.Tensor], name: str) -> list[torch.Tensor]:
+    if isinstance(ts, torch.Tensor):
+        if ts.dim() != 3:
+            raise ValueError(f"{name} as one tensor must be [R, T, H]")
+        ts = list(ts.unbind(0))
+    return list(ts)
+
+
+def sf_swizzled_shape(T: int, H: int) -> tuple[int, int]:
+    """Shape of the padded SWIZZLED_128x4 scale-factor buffer for [T, H] values."""
+    return (T + 127) // 128 * 128, (H // 16 + 3) // 4 * 4
+
+
+def new_outputs(pattern: int, T: int, H: int, device="cuda", partial_cols: int = 0,
+                sf_layout: int = SFLayout.LINEAR, with_allreduce_out: bool = False) -> dict:
+    """Allocate (torch.empty) the required outputs of a pattern."""
+    p = int(pattern)
+    e = lambda *s, dt=torch.bfloat16: torch.empty(s, dtype=dt, device=device)  # noqa: E731
+    out = {}
+    if p == 0 or with_allreduce_out:
+        out["allreduce_out"] = e(T, H)
+    if p != 0:
+        out["residual_out"] = e(T, H)
+    if p in (1, 4, 5):
+        out["norm_out"] = e(T, H)
+    if p in (7, 8):
+        out["partial_norm_out"] = e(T, partial_cols)
+    if p in (2, 4, 6, 7):
+        out["quant_out"] = e(T, H, dt=torch.uint8)
+    if p in (3, 5):
+        out["quant_out"] = e(T, H // 2, dt=torch.uint8)
+        shape = sf_swizzled_shape(T, H) if int(sf_layout) == SFLayout.SWIZZLED_128x4 else (T, H // 16)
+        out["scale_out"] = e(*shape, dt=torch.uint8)
+    if p in (6, 7):
+        out["scale_out"] = e(T, H // 128, dt=torch.float32)
+    return out
+
+
+def ts_fused_reduce_norm(pattern: int, partials, residual: torch.Tensor | None = None,
+                         gamma: torch.Tensor | None = None, eps: float = 1e-6,
+                         scale_factor: torch.Tensor | float | None = None, *,
+                         allreduce_out: torch.Tensor | None = None,
+                         residual_out: torch.Tensor | None = None,
+                         norm_out: torch.Tensor | None = None,
+                         partial_norm_out: torch.Tensor | None = None,
+                         quant_out: torch.Tensor | None = None,
+                         scale_out: torch.Tensor | None = None,
+                         sf_layout: int = SFLayout.LINEAR, stream=None) -> None:
+    """Run one AllReduceFusionPattern (see include/ts_fused_norm.h).
+
+    ``partials``: R CUDA bf16 tensors [T, H] (or one [R, T, H] tensor).
+    ``scale_factor``: device fp32 tensor of one element, or a Python float
+    (then copied to the device first, as trtllm.py's wrapper does).
+    ``partial_norm_out``'s width gives partial_cols.
+    """
+    parts = [_dev(p, "partials[%d]" % i, torch.bfloat16) for i, p in enumerate(_rows(partials, "partials"))]
+    T, H = parts[0].shape
+    for p in parts:
+        if p.shape != (T, H) or not p.is_contiguous():
+            raise ValueError("every partial must be a contiguous [T, H] tensor")
+    for name, t in (("residual", residual), ("gamma", gamma), ("allreduce_out", allreduce_out),
+                    ("residual_out", residual_out), ("norm_out", norm_out),
+                    ("partial_norm_out", partial_norm_out), ("quant_out", quant_out),
+                    ("scale_out", scale_out)):
+        if t is not None:
+            _dev(t, name)
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+    if scale_factor is not None and not isinstance(scale_factor, torch.Tensor):
+        scale_factor = torch.tensor([float(scale_factor)], dtype=torch.float32, device=parts[0].device)
+    if scale_factor is not None:
+        _dev(scale_factor, "scale_factor", torch.float32)
+    outs = TsOuts(_ptr(allreduce_out), _ptr(residual_out), _ptr(norm_out), _ptr(partial_norm_out),
+                  0 if partial_norm_out is None else int(partial_norm_out.shape[-1]),
+                  _ptr(quant_out), _ptr(scale_out), int(sf_layout), 0)
+    arr = (ctypes.c_void_p * len(parts))(*[p.data_ptr() for p in parts])
+    _check(library().ts_fused_reduce_norm(int(pattern), arr, len(parts), _ptr(residual), _ptr(gamma),
+                                          float(eps), _ptr(scale_factor), int(T), int(H),
+                                          ctypes.byref(outs), _stream(stream)))
+
+
+def ts_qk_norm_sharded(shards, q_shard: int, k_shard: int, q_weight: torch.Tensor,
+                       k_weight: torch.Tensor, eps: float = 1e-6, q_out: torch.Tensor | None = None,
+                       k_out: torch.Tensor | None = None, stream=None):
+    """Sharded MiniMax QK-RMSNorm (see include/ts_fused_norm.h).
+
+    ``shards``: R CUDA bf16 tensors [T, >= q_shard + k_shard] with unit column
+    stride (row stride taken from ``stride(0)``), or one [R, T, row] tensor.
+    Returns (q_out [T, R*q_shard], k_out [T, R*k_shard]), allocated if None.
+    """
+    sh = [_dev(s, "shards[%d]" % i, torch.bfloat16) for i, s in enumerate(_rows(shards, "shards"))]
+    T = sh[0].shape[0]
+    stride = sh[0].stride(0)
+    for s in sh:
+        if s.dim() != 2 or s.shape[0] != T or s.stride(1) != 1 or s.stride(0) != stride:
+            raise ValueError("shards must share T and the row stride, with unit column stride")
+        if s.shape[1] < q_shard + k_shard:
+            raise ValueError("a shard row is narrower than q_shard + k_shard")
+    R = len(sh)
+    _dev(q_weight, "q_weight", torch.bfloat16)
+    _dev(k_weight, "k_weight", torch.bfloat16)
+    if q_out is None:
+        q_out = torch.empty((T, R * q_shard), dtype=torch.bfloat16, device=sh[0].device)
+    if k_out is None:
+        k_out = torch.empty((T, R * k_shard), dtype=torch.bfloat16, device=sh[0].device)
+    for name, t in (("q_out", q_out), ("k_out", k_out)):
+        _dev(t, name, torch.bfloat16)
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError(f"{name} must be 2-D with unit column stride")
+    arr = (ctypes.c_void_p * R)(*[s.data_ptr() for s in sh])
+    _check(library().ts_qk_norm_sharded(arr, R, int(T), int(stride), int(q_shard), int(k_shard),
+                                        _ptr(q_weight), _ptr(k_weight), float(eps), _ptr(q_out),
+                                        int(q_out.stride(0)), _ptr(k_out), int(k_out.stride(0)),
+                                        _stream(stream)))
+    return q_out, k_out

@@ -1,0 +1,336 @@
+// The C ABI declared in include/ts_fused_norm.h: host-side argument checks,
+// then one kernel launch on the caller's stream.  No allocation, no state,
+// no synchronisation.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "ts_fused_norm.h"
+
+using tsfn::Epilogue;
+
+namespace {
+
+thread_local char g_detail[512];
+
+int fail(int status, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int ok()
+{
+    g_detail[0] = '\0';
+    return TS_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Span {
+    uintptr_t lo = 0, hi = 0;  // [lo, hi)
+    const char *name = "";
+};
+
+Span span(const void *p, int64_t bytes, const char *name)
+{
+    Span s;
+    s.lo = reinterpret_cast<uintptr_t>(p);
+    s.hi = s.lo + (uintptr_t)(bytes > 0 ? bytes : 0);
+    s.name = name;
+    return s;
+}
+
+bool overlap(const Span &a, const Span &b)
+{
+    if (a.lo == a.hi || b.lo == b.hi)
+        return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+// Which outputs each pattern writes: 'R' required, 'o' optional, '-' absent.
+// Columns: allreduce_out residual_out norm_out partial_norm_out quant_out scale_out.
+const char *const kOutputTable[9] = {
+    "R-----",  // 0 kAllReduce
+    "oRR---",  // 1 kARResidualRMSNorm
+    "oR--R-",  // 2 kARResidualRMSNormFP8Quant
+    "oR--RR",  // 3 kARResidualRMSNormFP4Quant
+    "oRR-R-",  // 4 kARResidualRMSNormOutFP8Quant
+    "oRR-RR",  // 5 kARResidualRMSNormOutFP4Quant
+    "oR--RR",  // 6 kARResidualRMSNormFP8BlockWiseQuant
+    "oR-RRR",  // 7 kARResidualRMSNormPartialOutFP8BlockWiseQuant
+    "oRoR--",  // 8 kARResidualRMSNormPartialOut
+};
+
+const char *const kOutputNames[6] = {"allreduce_out", "residual_out", "norm_out",
+                                     "partial_norm_out", "quant_out", "scale_out"};
+
+constexpr int64_t kMaxH = 16384;
+constexpr int64_t kMaxRows = 0x7FFFFFFFLL;
+
+}  // namespace
+
+extern "C" const char *ts_status_string(int status)
+{
+    switch (status) {
+    case TS_OK: return "TS_OK";
+    case TS_ERR_BAD_PATTERN: return "TS_ERR_BAD_PATTERN";
+    case TS_ERR_NULL: return "TS_ERR_NULL";
+    case TS_ERR_SHAPE: return "TS_ERR_SHAPE";
+    case TS_ERR_ALIGN: return "TS_ERR_ALIGN";
+    case TS_ERR_UNSUPPORTED: return "TS_ERR_UNSUPPORTED";
+    case TS_ERR_ALIAS: return "TS_ERR_ALIAS";
+    case TS_ERR_LAUNCH: return "TS_ERR_LAUNCH";
+    default: return "TS_ERR_UNKNOWN";
+    }
+}
+
+extern "C" const char *ts_last_error_detail(void) { return g_detail; }
+
+extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, int R,
+                                    const void *residual, const void *gamma, float eps,
+                                    const float *scale_factor, int64_t T, int64_t H,
+                                    const ts_outs_t *outs, void *stream)
+{
+    if (pattern < 0 || pattern > 8)
+        return fail(TS_ERR_BAD_PATTERN, "pattern %d is not an AllReduceFusionPattern code (0..8)", pattern);
+    if (outs == nullptr)
+        return fail(TS_ERR_NULL, "outs is NULL");
+    if (partials == nullptr)
+        return fail(TS_ERR_NULL, "partials is NULL");
+    if (R < 1 || R > tsfn::kMaxR)
+        return fail(TS_ERR_SHAPE, "R = %d outside 1..%d", R, tsfn::kMaxR);
+    if (T < 0 || T > kMaxRows)
+        return fail(TS_ERR_SHAPE, "T = %lld outside 0..%lld", (long long)T, (long long)kMaxRows);
+    if (H < 8 || H % 8 != 0)
+        return fail(TS_ERR_SHAPE, "H = %lld must be a positive multiple of 8", (long long)H);
+    if (H > kMaxH)
+        return fail(TS_ERR_UNSUPPORTED, "H = %lld above the supported maximum %lld", (long long)H,
+                    (long long)kMaxH);
+    if ((pattern == 6 || pattern == 7) && H % 128 != 0)
+        return fail(TS_ERR_SHAPE, "FP8 1x128 blockwise needs H %% 128 == 0 (H = %lld)", (long long)H);
+    if ((pattern == 3 || pattern == 5) && H % 16 != 0)
+        return fail(TS_ERR_SHAPE, "NVFP4 needs H %% 16 == 0 (H = %lld)", (long long)H);
+    if (outs->reserved != 0)
+        return fail(TS_ERR_UNSUPPORTED, "ts_outs_t.reserved must be 0");
+
+    // inputs
+    for (int r = 0; r < R; ++r) {
+        if (partials[r] == nullptr)
+            return fail(TS_ERR_NULL, "partials[%d] is NULL", r);
+        if (!aligned(partials[r], 16))
+            return fail(TS_ERR_ALIGN, "partials[%d] is not 16-byte aligned", r);
+    }
+    if (pattern != 0) {
+        if (residual == nullptr)
+            return fail(TS_ERR_NULL, "residual is NULL (required for pattern %d)", pattern);
+        if (gamma == nullptr)
+            return fail(TS_ERR_NULL, "gamma is NULL (required for pattern %d)", pattern);
+        if (!aligned(residual, 16))
+            return fail(TS_ERR_ALIGN, "residual is not 16-byte aligned");
+        if (!aligned(gamma, 16))
+            return fail(TS_ERR_ALIGN, "gamma is not 16-byte aligned");
+    }
+    const bool needs_scale = pattern >= 2 && pattern <= 5;
+    if (needs_scale) {
+        if (scale_factor == nullptr)
+            return fail(TS_ERR_NULL, "scale_factor is NULL (required for pattern %d)", pattern);
+        if (!aligned(scale_factor, 4))
+            return fail(TS_ERR_ALIGN, "scale_factor is not 4-byte aligned");
+    }
+
+    // outputs against the pattern's table
+    void *const out_ptr[6] = {outs->allreduce_out, outs->residual_out, outs->norm_out,
+                              outs->partial_norm_out, outs->quant_out, outs->scale_out};
+    const char *row = kOutputTable[pattern];
+    for (int i = 0; i < 6; ++i) {
+        if (row[i] == 'R' && out_ptr[i] == nullptr)
+            return fail(TS_ERR_NULL, "%s is required for pattern %d", kOutputNames[i], pattern);
+        if (row[i] == '-' && out_ptr[i] != nullptr)
+            return fail(TS_ERR_UNSUPPORTED, "%s is not an output of pattern %d (pass NULL)",
+                        kOutputNames[i], pattern);
+        const uintptr_t need = (i == 5) ? 4 : 16;
+        if (out_ptr[i] != nullptr && !aligned(out_ptr[i], need))
+            return fail(TS_ERR_ALIGN, "%s is not %d-byte aligned", kOutputNames[i], (int)need);
+    }
+    const bool fp4 = pattern == 3 || pattern == 5;
+    const bool fp8_block = pattern == 6 || pattern == 7;
+    const bool partial = pattern == 7 || pattern == 8;
+    int64_t P = 0;
+    if (partial) {
+        P = outs->partial_cols;
+        if (P <= 0 || P > H || P % 8 != 0)
+            return fail(TS_ERR_SHAPE, "partial_cols = %lld must be in 1..H and a multiple of 8",
+                        (long long)P);
+    }
+    bool swz = false;
+    if (fp4) {
+        if (outs->sf_layout == TS_SF_SWIZZLED_128x4)
+            swz = true;
+        else if (outs->sf_layout == TS_SF_SWIZZLED_8x4)
+            return fail(TS_ERR_UNSUPPORTED, "SF layout SWIZZLED_8x4 is not implemented");
+        else if (outs->sf_layout != TS_SF_LINEAR)
+            return fail(TS_ERR_BAD_PATTERN, "sf_layout %d is not a QuantizationSFLayout code",
+                        (int)outs->sf_layout);
+    }
+
+    // aliasing: outputs disjoint from each other and from the inputs, except
+    // allreduce_out == partials[0] and residual_out == residual (in place)
+    const int64_t elems = T * H;
+    const int64_t n_sf = H / 16;
+    const int64_t sf_rows = swz ? (T + 127) / 128 * 128 : T;
+    const int64_t sf_cols = swz ? (n_sf + 3) / 4 * 4 : n_sf;
+    int64_t quant_bytes = fp4 ? elems / 2 : elems;
+    int64_t scale_bytes = fp4 ? sf_rows * sf_cols : (fp8_block ? T * (H / 128) * 4 : 0);
+    const int64_t out_bytes[6] = {elems * 2, elems * 2, elems * 2, T * P * 2, quant_bytes, scale_bytes};
+    Span outs_s[6];
+    for (int i = 0; i < 6; ++i)
+        outs_s[i] = span(out_ptr[i], out_ptr[i] ? out_bytes[i] : 0, kOutputNames[i]);
+    for (int i = 0; i < 6; ++i)
+        for (int j = i + 1; j < 6; ++j)
+            if (overlap(outs_s[i], outs_s[j]))
+                return fail(TS_ERR_ALIAS, "%s overlaps %s", outs_s[i].name, outs_s[j].name);
+    for (int i = 0; i < 6; ++i) {
+        if (out_ptr[i] == nullptr)
+            continue;
+        for (int r = 0; r < R; ++r) {
+            if (i == 0 && r == 0 && out_ptr[0] == partials[0])
+                continue;
+            if (overlap(outs_s[i], span(partials[r], elems * 2, "")))
+                return fail(TS_ERR_ALIAS, "%s overlaps partials[%d]", kOutputNames[i], r);
+        }
+        if (pattern != 0) {
+            if (!(i == 1 && out_ptr[1] == residual) && overlap(outs_s[i], span(residual, elems * 2, "")))
+                return fail(TS_ERR_ALIAS, "%s overlaps residual", kOutputNames[i]);
+            if (overlap(outs_s[i], span(gamma, H * 2, "")))
+                return fail(TS_ERR_ALIAS, "%s overlaps gamma", kOutputNames[i]);
+        }
+        if (needs_scale && overlap(outs_s[i], span(scale_factor, 4, "")))
+            return fail(TS_ERR_ALIAS, "%s overlaps scale_factor", kOutputNames[i]);
+    }
+
+    if (T == 0)
+        return ok();
+
+    tsfn::FusedArgs a{};
+    for (int r = 0; r < R; ++r)
+        a.partials[r] = static_cast<const uint16_t *>(partials[r]);
+    a.R = R;
+    a.residual = static_cast<const uint16_t *>(residual);
+    a.gamma = static_cast<const uint16_t *>(gamma);
+    a.eps = eps;
+    a.scale_factor = needs_scale ? scale_factor : nullptr;
+    a.T = T;
+    a.H = H;
+    a.allreduce_out = static_cast<uint16_t *>(outs->allreduce_out);
+    a.residual_out = static_cast<uint16_t *>(outs->residual_out);
+    a.norm_out = static_cast<uint16_t *>(outs->norm_out);
+    a.partial_norm_out = static_cast<uint16_t *>(outs->partial_norm_out);
+    a.partial_cols = P;
+    a.quant_out = static_cast<uint8_t *>(outs->quant_out);
+    a.scale_out = outs->scale_out;
+    a.sf_swizzled = swz ? 1 : 0;
+    a.sf_rows = sf_rows;
+    a.sf_cols = sf_cols;
+
+    Epilogue ep;
+    switch (pattern) {
+    case 0: ep = Epilogue::kAllReduce; break;
+    case 1:
+    case 8: ep = Epilogue::kNorm; break;
+    case 2:
+    case 4: ep = Epilogue::kFp8Tensor; break;
+    case 3:
+    case 5: ep = Epilogue::kFp4; break;
+    default: ep = Epilogue::kFp8Block; break;
+    }
+    const cudaError_t err = tsfn::launch_fused(ep, a, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess)
+        return fail(TS_ERR_LAUNCH, "kernel launch failed: %s (%s)", cudaGetErrorName(err),
+                    cudaGetErrorString(err));
+    return ok();
+}
+
+extern "C" int ts_qk_norm_sharded(const void *const *qkv_shards, int R, int64_t T,
+                                  int64_t row_stride, int64_t q_shard, int64_t k_shard,
+                                  const void *q_weight, const void *k_weight, float eps,
+                                  void *q_out, int64_t ldq, void *k_out, int64_t ldk, void *stream)
+{
+    if (qkv_shards == nullptr)
+        return fail(TS_ERR_NULL, "qkv_shards is NULL");
+    if (R < 1 || R > tsfn::kMaxR)
+        return fail(TS_ERR_SHAPE, "R = %d outside 1..%d", R, tsfn::kMaxR);
+    if (T < 0 || T > kMaxRows)
+        return fail(TS_ERR_SHAPE, "T = %lld outside 0..%lld", (long long)T, (long long)kMaxRows);
+    if (q_shard < 8 || q_shard % 8 != 0 || k_shard < 8 || k_shard % 8 != 0)
+        return fail(TS_ERR_SHAPE, "q_shard = %lld and k_shard = %lld must be positive multiples of 8",
+                    (long long)q_shard, (long long)k_shard);
+    if (q_shard > 4096 || k_shard > 1024)
+        return fail(TS_ERR_UNSUPPORTED, "q_shard <= 4096 and k_shard <= 1024 are supported");
+    if (row_stride % 8 != 0 || row_stride < q_shard + k_shard)
+        return fail(TS_ERR_SHAPE, "row_stride = %lld must be a multiple of 8 and >= q_shard + k_shard",
+                    (long long)row_stride);
+    if (ldq % 8 != 0 || ldq < R * q_shard)
+        return fail(TS_ERR_SHAPE, "ldq = %lld must be a multiple of 8 and >= R*q_shard", (long long)ldq);
+    if (ldk % 8 != 0 || ldk < R * k_shard)
+        return fail(TS_ERR_SHAPE, "ldk = %lld must be a multiple of 8 and >= R*k_shard", (long long)ldk);
+    for (int r = 0; r < R; ++r) {
+        if (qkv_shards[r] == nullptr)
+            return fail(TS_ERR_NULL, "qkv_shards[%d] is NULL", r);
+        if (!aligned(qkv_shards[r], 16))
+            return fail(TS_ERR_ALIGN, "qkv_shards[%d] is not 16-byte aligned", r);
+    }
+    const void *const ptrs[4] = {q_weight, k_weight, q_out, k_out};
+    const char *const names[4] = {"q_weight", "k_weight", "q_out", "k_out"};
+    for (int i = 0; i < 4; ++i) {
+        if (ptrs[i] == nullptr)
+            return fail(TS_ERR_NULL, "%s is NULL", names[i]);
+        if (!aligned(ptrs[i], 16))
+            return fail(TS_ERR_ALIGN, "%s is not 16-byte aligned", names[i]);
+    }
+    if (T > 0) {
+        const Span qo = span(q_out, ((T - 1) * ldq + R * q_shard) * 2, "q_out");
+        const Span ko = span(k_out, ((T - 1) * ldk + R * k_shard) * 2, "k_out");
+        if (overlap(qo, ko))
+            return fail(TS_ERR_ALIAS, "q_out overlaps k_out");
+        const Span ins[2] = {span(q_weight, R * q_shard * 2, "q_weight"),
+                             span(k_weight, R * k_shard * 2, "k_weight")};
+        for (const Span &o : {qo, ko}) {
+            for (const Span &in : ins)
+                if (overlap(o, in))
+                    return fail(TS_ERR_ALIAS, "%s overlaps %s", o.name, in.name);
+            for (int r = 0; r < R; ++r)
+                if (overlap(o, span(qkv_shards[r], ((T - 1) * row_stride + q_shard + k_shard) * 2, "")))
+                    return fail(TS_ERR_ALIAS, "%s overlaps qkv_shards[%d]", o.name, r);
+        }
+    }
+    if (T == 0)
+        return ok();
+
+    tsfn::QKArgs a{};
+    for (int r = 0; r < R; ++r)
+        a.shards[r] = static_cast<const uint16_t *>(qkv_shards[r]);
+    a.R = R;
+    a.T = T;
+    a.row_stride = row_stride;
+    a.Q = (int)q_shard;
+    a.K = (int)k_shard;
+    a.q_weight = static_cast<const uint16_t *>(q_weight);
+    a.k_weight = static_cast<const uint16_t *>(k_weight);
+    a.eps = eps;
+    a.q_out = static_cast<uint16_t *>(q_out);
+    a.ldq = ldq;
+    a.k_out = static_cast<uint16_t *>(k_out);
+    a.ldk = ldk;
+    const cudaError_t err = tsfn::launch_qk(a, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess)
+        return fail(TS_ERR_LAUNCH, "kernel launch failed: %s (%s)", cudaGetErrorName(err),
+                    cudaGetErrorString(err));
+    return ok();
+}

@@ -1,0 +1,157 @@
+// Device helpers shared by the kernels: 128-bit global access, bf16 <-> fp32,
+// and the FP8 E4M3 / FP4 E2M1 conversions (hardware cvt with round-to-nearest-
+// even and saturation to the largest finite value).
+#pragma once
+
+#include <cstdint>
+
+namespace tsfn {
+
+// ---------------------------------------------------------------------------
+// 128-bit loads / stores
+// ---------------------------------------------------------------------------
+
+// Streaming load: data read exactly once (partials, residual, shard rows).
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Read-only, reused across rows (gamma, q/k weights): keep in L1/L2.
+__device__ __forceinline__ uint4 ld_keep(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void *p, uint4 v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_v2(void *p, uint2 v)
+{
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_u32(void *p, uint32_t v)
+{
+    asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_u8(void *p, uint32_t v)
+{
+    asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_f32(void *p, float v)
+{
+    asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// bf16 <-> fp32
+// ---------------------------------------------------------------------------
+
+// Widen the two bf16 halves of a 32-bit word (exact: bf16 is the high half of
+// an fp32 bit pattern).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
+{
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// Round two fp32 values to bf16 (nearest, ties to even); lo in bits 0..15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8])
+{
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
+// ---------------------------------------------------------------------------
+// FP8 E4M3 and FP4 E2M1
+// ---------------------------------------------------------------------------
+
+// Two fp32 -> two E4M3 codes (nearest-even, saturating to +-448); lo in bits 0..7.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Eight fp32 -> eight E4M3 codes, element i in byte i.
+__device__ __forceinline__ uint2 cvt_e4m3x8(const float (&f)[8])
+{
+    uint2 r;
+    r.x = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
+    r.y = cvt_e4m3x2(f[4], f[5]) | (cvt_e4m3x2(f[6], f[7]) << 16);
+    return r;
+}
+
+// Two fp32 -> two E2M1 codes (nearest-even, saturating to +-6); lo in bits 0..3.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Eight fp32 -> eight E2M1 codes packed in 32 bits, element i in nibble i.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&f)[8])
+{
+    return cvt_e2m1x2(f[0], f[1]) | (cvt_e2m1x2(f[2], f[3]) << 8) |
+           (cvt_e2m1x2(f[4], f[5]) << 16) | (cvt_e2m1x2(f[6], f[7]) << 24);
+}
+
+// One fp32 -> one E4M3 code.
+__device__ __forceinline__ uint32_t cvt_e4m3(float v) { return cvt_e4m3x2(v, 0.0f) & 0xFFu; }
+
+// Value of an E4M3 code (FN variant: bias 7; exponent field 0 is subnormal,
+// f * 2^-9).  Codes 0x7F/0xFF (NaN) never come out of a saturating cvt.
+__device__ __forceinline__ float e4m3_value(uint32_t c)
+{
+    const uint32_t e = (c >> 3) & 0xFu, f = c & 0x7u;
+    float mag = e ? __uint_as_float(((e + 120u) << 23) | (f << 20))
+                  : __int2float_rn((int)f) * 0.001953125f;  // 2^-9
+    return (c & 0x80u) ? -mag : mag;
+}
+
+// ---------------------------------------------------------------------------
+// reductions
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace tsfn

@@ -1,0 +1,267 @@
+// Fused reduce -> residual -> RMSNorm -> {bf16 | FP8 | NVFP4} epilogue,
+// one CTA per token row.
+//
+// The math is the one of tokenspeed triton.py `amd_allreduce_residual_rmsnorm_kernel`
+// (and `amd_all_reduce_kernel` for kAllReduce): the R partials are widened to
+// fp32 and added in ascending order into an accumulator that starts at +0,
+// the residual is added in fp32, the row's mean of squares of that unrounded
+// fp32 x gives s = rsqrt(mean + eps), and n = bf16((x * s) * gamma).  The
+// quantisers of trtllm.py `AllReduceFusionPattern` then read n:
+//   FP8 per tensor   code = e4m3(n * sigma)
+//   FP8 1x128 block  s_g = amax/448, code = e4m3(n / s_g)  (0 if s_g == 0)
+//   NVFP4 16-block   SF = e4m3(g * (amax/6)), code = e2m1(n * (g / value(SF)))
+//
+// Layout of the work: row t is H/8 chunks of 8 bf16 (16 bytes).  Thread i of
+// the CTA owns chunks i, i + blockDim, ... (V of them), so a warp covers 32
+// consecutive chunks = 512 contiguous bytes of every tensor; a 1x128 FP8 group
+// is 16 consecutive lanes and an NVFP4 block 2 consecutive lanes, so the group
+// maxima are warp shuffles.  x stays in registers between the two phases; the
+// only shared memory is the per-warp partial sums of x^2.
+#include "device_util.cuh"
+#include "launch.h"
+
+namespace tsfn {
+
+namespace {
+
+constexpr int kMaxThreads = 512;
+
+__device__ __forceinline__ int64_t sf_offset(const FusedArgs &a, int64_t m, int64_t k)
+{
+    if (!a.sf_swizzled)
+        return m * (a.H >> 4) + k;
+    // 512-byte tiles of 128 rows x 4 columns; inside a tile row m%128 = 32*i + j
+    // sits at 16*j + 4*i.
+    const int64_t tiles_per_band = a.sf_cols >> 2;
+    return ((m >> 7) * tiles_per_band + (k >> 2)) * 512 + (m & 31) * 16 + ((m & 127) >> 5) * 4 +
+           (k & 3);
+}
+
+template <int RB, int V, Epilogue EP>
+__global__ void __launch_bounds__(kMaxThreads) fused_rows_kernel(const __grid_constant__ FusedArgs a)
+{
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const int lane = tid & 31;
+    const int64_t row = blockIdx.x;
+    const int nc = (int)(a.H >> 3);
+
+    if constexpr (EP == Epilogue::kFp4) {
+        if (row >= a.T) {  // a padding row of the swizzled SF buffer: zeros only
+            uint8_t *sf = static_cast<uint8_t *>(a.scale_out);
+            for (int64_t k4 = tid; k4 < (a.sf_cols >> 2); k4 += nthr)
+                st_u32(sf + sf_offset(a, row, k4 * 4), 0u);
+            return;
+        }
+    }
+
+    const int64_t rbase = row * a.H;
+    float x[V][8];
+    float ss = 0.0f;
+
+    // ---- phase 1: sum of partials (+ residual), sum of squares ------------
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = tid + v * nthr;
+        if (c < nc) {
+            const int64_t off = rbase + (int64_t)c * 8;
+            uint4 raw[RB];
+#pragma unroll
+            for (int r = 0; r < RB; ++r)
+                if (r < a.R)
+                    raw[r] = ld_stream(a.partials[r] + off);
+            uint4 res;
+            if constexpr (EP != Epilogue::kAllReduce)
+                res = ld_stream(a.residual + off);
+            float acc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[e] = 0.0f;
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                if (r < a.R) {
+                    float f[8];
+                    unpack8(raw[r], f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        acc[e] = __fadd_rn(acc[e], f[e]);
+                }
+            }
+            if (EP == Epilogue::kAllReduce || a.allreduce_out != nullptr)
+                st_v4(a.allreduce_out + off, pack8(acc));
+            if constexpr (EP != Epilogue::kAllReduce) {
+                float f[8];
+                unpack8(res, f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    x[v][e] = __fadd_rn(acc[e], f[e]);
+                    ss = fmaf(x[v][e], x[v][e], ss);
+                }
+                st_v4(a.residual_out + off, pack8(x[v]));
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                x[v][e] = 0.0f;
+        }
+    }
+    if constexpr (EP == Epilogue::kAllReduce)
+        return;
+
+    // ---- row reduction of x^2 (same order in every thread) -----------------
+    __shared__ float red[kMaxThreads / 32];
+    ss = warp_sum(ss);
+    if (lane == 0)
+        red[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int w = 0; w < (nthr >> 5); ++w)
+        tot += red[w];
+    const float scale = rsqrtf(__fadd_rn(__fdiv_rn(tot, (float)a.H), a.eps));
+
+    float qscale = 0.0f;
+    if constexpr (EP == Epilogue::kFp8Tensor || EP == Epilogue::kFp4)
+        qscale = __ldg(a.scale_factor);
+
+    // ---- phase 2: norm and the pattern's outputs ----------------------------
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        const int c = tid + v * nthr;
+        const bool live = c < nc;
+        const int64_t off = rbase + (int64_t)c * 8;
+        float nf[8];
+        uint4 nb = make_uint4(0, 0, 0, 0);
+        if (live) {
+            float g[8];
+            unpack8(ld_keep(a.gamma + (int64_t)c * 8), g);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                nf[e] = __fmul_rn(__fmul_rn(x[v][e], scale), g[e]);
+            nb = pack8(nf);
+            // quantisers read the bf16-rounded n
+            unpack8(nb, nf);
+            if (a.norm_out != nullptr)
+                st_v4(a.norm_out + off, nb);
+            if (a.partial_norm_out != nullptr && (int64_t)c * 8 < a.partial_cols)
+                st_v4(a.partial_norm_out + row * a.partial_cols + (int64_t)c * 8, nb);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                nf[e] = 0.0f;
+        }
+
+        if constexpr (EP == Epilogue::kFp8Tensor) {
+            if (live) {
+                float q[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    q[e] = __fmul_rn(nf[e], qscale);
+                st_v2(a.quant_out + off, cvt_e4m3x8(q));
+            }
+        } else if constexpr (EP == Epilogue::kFp8Block) {
+            float amax = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                amax = fmaxf(amax, fabsf(nf[e]));
+            // 16 lanes = 128 columns; all 32 lanes take part in the shuffles
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float sg = __fdiv_rn(amax, 448.0f);
+            if (live) {
+                if ((c & 15) == 0)
+                    st_f32(static_cast<float *>(a.scale_out) + row * (a.H >> 7) + (c >> 4), sg);
+                uint2 codes = make_uint2(0, 0);
+                if (sg != 0.0f) {
+                    float q[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        q[e] = __fdiv_rn(nf[e], sg);
+                    codes = cvt_e4m3x8(q);
+                }
+                st_v2(a.quant_out + off, codes);
+            }
+        } else if constexpr (EP == Epilogue::kFp4) {
+            float amax = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                amax = fmaxf(amax, fabsf(nf[e]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // 16-element block
+            const uint32_t sf = cvt_e4m3(__fmul_rn(qscale, __fdiv_rn(amax, 6.0f)));
+            const float d = e4m3_value(sf);
+            uint32_t codes = 0;
+            if (d != 0.0f) {
+                const float es = __fdiv_rn(qscale, d);
+                float q[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    q[e] = __fmul_rn(nf[e], es);
+                codes = cvt_e2m1x8(q);
+            }
+            if (live)
+                st_u32(a.quant_out + (rbase >> 1) + (int64_t)c * 4, codes);
+            // scale factors: SF k = c/2 lives on the even lane; lanes with
+            // c % 8 == 0 gather 4 consecutive SFs into one 32-bit store.
+            const uint32_t s2 = __shfl_down_sync(0xffffffffu, sf, 2);
+            const uint32_t s4 = __shfl_down_sync(0xffffffffu, sf, 4);
+            const uint32_t s6 = __shfl_down_sync(0xffffffffu, sf, 6);
+            uint8_t *sfp = static_cast<uint8_t *>(a.scale_out);
+            const int64_t k = c >> 1;
+            if (live) {
+                if ((a.H & 63) == 0) {
+                    if ((lane & 7) == 0)
+                        st_u32(sfp + sf_offset(a, row, k), sf | (s2 << 8) | (s4 << 16) | (s6 << 24));
+                } else if ((c & 1) == 0) {
+                    st_u8(sfp + sf_offset(a, row, k), sf);
+                }
+            }
+        }
+    }
+
+    if constexpr (EP == Epilogue::kFp4) {
+        // zero the padding columns of this row in the swizzled layout
+        if (a.sf_swizzled && tid == 0) {
+            uint8_t *sfp = static_cast<uint8_t *>(a.scale_out);
+            for (int64_t k = a.H >> 4; k < a.sf_cols; ++k)
+                st_u8(sfp + sf_offset(a, row, k), 0u);
+        }
+    }
+}
+
+template <int RB, int V>
+cudaError_t launch_rb_v(Epilogue ep, const FusedArgs &a, int nthr, int64_t grid, cudaStream_t s)
+{
+    const dim3 g((unsigned)grid), b((unsigned)nthr);
+    switch (ep) {
+    case Epilogue::kAllReduce: fused_rows_kernel<RB, V, Epilogue::kAllReduce><<<g, b, 0, s>>>(a); break;
+    case Epilogue::kNorm: fused_rows_kernel<RB, V, Epilogue::kNorm><<<g, b, 0, s>>>(a); break;
+    case Epilogue::kFp8Tensor: fused_rows_kernel<RB, V, Epilogue::kFp8Tensor><<<g, b, 0, s>>>(a); break;
+    case Epilogue::kFp4: fused_rows_kernel<RB, V, Epilogue::kFp4><<<g, b, 0, s>>>(a); break;
+    case Epilogue::kFp8Block: fused_rows_kernel<RB, V, Epilogue::kFp8Block><<<g, b, 0, s>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+template <int RB>
+cudaError_t launch_rb(Epilogue ep, const FusedArgs &a, cudaStream_t s)
+{
+    const int nc = (int)(a.H >> 3);
+    const int V = nc <= kMaxThreads ? 1 : (nc <= 2 * kMaxThreads ? 2 : 4);
+    const int per = (nc + V - 1) / V;
+    const int nthr = (per + 31) / 32 * 32;
+    const int64_t grid = (ep == Epilogue::kFp4 && a.sf_swizzled) ? a.sf_rows : a.T;
+    if (V == 1) return launch_rb_v<RB, 1>(ep, a, nthr, grid, s);
+    if (V == 2) return launch_rb_v<RB, 2>(ep, a, nthr, grid, s);
+    return launch_rb_v<RB, 4>(ep, a, nthr, grid, s);
+}
+
+}  // namespace
+
+cudaError_t launch_fused(Epilogue ep, const FusedArgs &a, cudaStream_t stream)
+{
+    if (a.R <= 4) return launch_rb<4>(ep, a, stream);
+    if (a.R <= 8) return launch_rb<8>(ep, a, stream);
+    return launch_rb<16>(ep, a, stream);
+}
+
+}  // namespace tsfn

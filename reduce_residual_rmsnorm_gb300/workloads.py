@@ -67,27 +67,30 @@ WORKLOADS = {
 
 
 def _normal(shape, std, g, outlier_frac=0.0, outlier_mul=50.0):
-    x = torch.randn(shape, generator=g, dtype=torch.float32)
+    x = torch.randn(shape, generator=g, dtype=torch.float32, device=g.device)
     if std != 1.0:
         x.mul_(std)
     if outlier_frac > 0.0:
         numel = x.numel()
         k = int(round(outlier_frac * numel))
-        idx = torch.randint(0, numel, (k,), generator=g)
+        idx = torch.randint(0, numel, (k,), generator=g, device=g.device)
         x.view(-1)[idx] *= outlier_mul
     return x.to(BF16)
 
 
 def _uniform(shape, lo, hi, g):
-    return (torch.rand(shape, generator=g, dtype=torch.float32) * (hi - lo) + lo).to(BF16)
+    return (torch.rand(shape, generator=g, dtype=torch.float32, device=g.device) * (hi - lo) + lo).to(BF16)
 
 
-def fused_inputs(shape: FusedShape, seed: int = 0) -> dict:
-    """Host bf16 tensors: ``partials`` [R, T, H], ``residual`` [T, H], ``gamma`` [H]."""
-    g = torch.Generator(device="cpu")
+def fused_inputs(shape: FusedShape, seed: int = 0, device="cpu") -> dict:
+    """bf16 tensors ``partials`` [R, T, H], ``residual`` [T, H], ``gamma`` [H].
+
+    Drawn with a generator on ``device`` (host by default; the host and a
+    CUDA generator give different, equally seeded, numbers)."""
+    g = torch.Generator(device=device)
     g.manual_seed(seed)
     R, T, H = shape.R, shape.T, shape.H
-    partials = torch.empty((R, T, H), dtype=BF16)
+    partials = torch.empty((R, T, H), dtype=BF16, device=device)
     for r in range(R):
         partials[r] = _normal((T, H), shape.p_std, g, shape.outlier_frac, shape.outlier_mul)
     residual = _normal((T, H), shape.res_std, g, shape.outlier_frac, shape.outlier_mul)
@@ -95,13 +98,13 @@ def fused_inputs(shape: FusedShape, seed: int = 0) -> dict:
     return {"partials": partials, "residual": residual, "gamma": gamma}
 
 
-def qk_inputs(shape: QKShape, seed: int = 0) -> dict:
-    """Host bf16 tensors: ``shards`` [R, T, row_stride], ``q_weight`` [R*q_shard],
-    ``k_weight`` [R*k_shard]."""
-    g = torch.Generator(device="cpu")
+def qk_inputs(shape: QKShape, seed: int = 0, device="cpu") -> dict:
+    """bf16 tensors ``shards`` [R, T, row_stride], ``q_weight`` [R*q_shard],
+    ``k_weight`` [R*k_shard], drawn with a generator on ``device``."""
+    g = torch.Generator(device=device)
     g.manual_seed(seed)
     R, T = shape.R, shape.T
-    shards = torch.empty((R, T, shape.row_stride), dtype=BF16)
+    shards = torch.empty((R, T, shape.row_stride), dtype=BF16, device=device)
     for r in range(R):
         shards[r] = _normal((T, shape.row_stride), 1.0, g)
     q_weight = _uniform((R * shape.q_shard,), 0.5, 1.5, g)

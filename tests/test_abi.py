@@ -1,0 +1,230 @@
+"""The C ABI without a GPU: the library loads, exports every function the header
+declares, and rejects bad arguments on the host before any launch.
+
+Every negative case below carries exactly one defect that the host checks
+catch, so no kernel is ever launched (the pointers are fake addresses that are
+never dereferenced).  The one accepted case has T = 0, which validates and
+returns without launching.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import reduce_residual_rmsnorm_gb300 as pkg
+from reduce_residual_rmsnorm_gb300 import build as libbuild
+from reduce_residual_rmsnorm_gb300._binding import TsOuts
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+TS_OK, BAD_PATTERN, NULL, SHAPE, ALIGN, UNSUPPORTED, ALIAS = 0, -1, -2, -3, -4, -5, -6
+MiB = 1 << 20
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return pkg.library()
+
+
+def _header_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\bTS_API\s+[\w\s\*]*?\b(ts_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_api():
+    assert _header_functions() == sorted(pkg.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in ((0, "TS_OK"), (-1, "TS_ERR_BAD_PATTERN"), (-2, "TS_ERR_NULL"), (-3, "TS_ERR_SHAPE"),
+                       (-4, "TS_ERR_ALIGN"), (-5, "TS_ERR_UNSUPPORTED"), (-6, "TS_ERR_ALIAS"),
+                       (-7, "TS_ERR_LAUNCH"), (-99, "TS_ERR_UNKNOWN")):
+        assert lib.ts_status_string(code).decode() == name
+
+
+# ---------------------------------------------------------------------------
+# ts_fused_reduce_norm
+# ---------------------------------------------------------------------------
+
+class Fake:
+    """Distinct, 16-byte aligned, non-overlapping fake device addresses."""
+
+    def __init__(self):
+        self.next = 0x7F0000000000
+
+    def __call__(self, nbytes=64 * MiB):
+        p = self.next
+        self.next += (nbytes + 4095) // 4096 * 4096 + 4096
+        return p
+
+
+def _fused_call(lib, pattern=1, R=2, T=16, H=256, P=0, sf_layout=2, mutate=None):
+    f = Fake()
+    parts = [f() for _ in range(R)]
+    args = dict(pattern=pattern, partials=parts, R=R, residual=f(), gamma=f(), eps=1e-6,
+                scale_factor=f(), T=T, H=H)
+    table = {0: "R-----", 1: "oRR---", 2: "oR--R-", 3: "oR--RR", 4: "oRR-R-", 5: "oRR-RR",
+             6: "oR--RR", 7: "oR-RRR", 8: "oRoR--"}
+    row = table.get(pattern, "oRR---")
+    keys = ["allreduce_out", "residual_out", "norm_out", "partial_norm_out", "quant_out", "scale_out"]
+    outs = {k: (f() if row[i] == "R" else None) for i, k in enumerate(keys)}
+    outs["partial_cols"] = P
+    outs["sf_layout"] = sf_layout
+    outs["reserved"] = 0
+    if mutate:
+        mutate(args, outs)
+    o = TsOuts(outs["allreduce_out"], outs["residual_out"], outs["norm_out"], outs["partial_norm_out"],
+               outs["partial_cols"], outs["quant_out"], outs["scale_out"], outs["sf_layout"], outs["reserved"])
+    parts = args["partials"]
+    arr = None if parts is None else (ctypes.c_void_p * len(parts))(*parts)
+    st = lib.ts_fused_reduce_norm(args["pattern"], arr, args["R"], args["residual"], args["gamma"],
+                                  args["eps"], args["scale_factor"], args["T"], args["H"],
+                                  ctypes.byref(o), None)
+    return st, lib.ts_last_error_detail().decode()
+
+
+def test_zero_rows_is_a_valid_no_op(lib):
+    for pattern, H, P in ((0, 256, 0), (1, 256, 0), (2, 256, 0), (3, 256, 0), (5, 256, 0), (6, 256, 0),
+                          (7, 256, 128), (8, 256, 64)):
+        st, detail = _fused_call(lib, pattern=pattern, T=0, H=H, P=P)
+        assert st == TS_OK, (pattern, detail)
+
+
+def _set(path, value):
+    def m(args, outs):
+        (args if path in args else outs)[path] = value
+    return m
+
+
+NEG_FUSED = [
+    ("pattern -1", dict(pattern=-1), BAD_PATTERN),
+    ("pattern 9", dict(pattern=9), BAD_PATTERN),
+    ("R = 0", dict(mutate=lambda a, o: a.update(R=0)), SHAPE),
+    ("R = 17", dict(R=17), SHAPE),
+    ("T < 0", dict(T=-1), SHAPE),
+    ("H = 0", dict(H=0), SHAPE),
+    ("H % 8", dict(H=100), SHAPE),
+    ("H too large", dict(H=16392), UNSUPPORTED),
+    ("blockwise H % 128", dict(pattern=6, H=192), SHAPE),
+    ("fp4 H % 16", dict(pattern=3, H=200), SHAPE),
+    ("partials NULL", dict(mutate=_set("partials", None)), NULL),
+    ("a partial NULL", dict(mutate=lambda a, o: a["partials"].__setitem__(1, None)), NULL),
+    ("partial misaligned", dict(mutate=lambda a, o: a["partials"].__setitem__(0, a["partials"][0] + 2)), ALIGN),
+    ("residual NULL", dict(mutate=_set("residual", None)), NULL),
+    ("gamma NULL", dict(mutate=_set("gamma", None)), NULL),
+    ("gamma misaligned", dict(mutate=lambda a, o: a.update(gamma=a["gamma"] + 8)), ALIGN),
+    ("scale NULL fp8", dict(pattern=2, mutate=_set("scale_factor", None)), NULL),
+    ("scale NULL fp4", dict(pattern=3, mutate=_set("scale_factor", None)), NULL),
+    ("scale misaligned", dict(pattern=2, mutate=lambda a, o: a.update(scale_factor=a["scale_factor"] + 2)), ALIGN),
+    ("residual_out NULL", dict(mutate=_set("residual_out", None)), NULL),
+    ("norm_out NULL", dict(mutate=_set("norm_out", None)), NULL),
+    ("allreduce_out NULL p0", dict(pattern=0, mutate=_set("allreduce_out", None)), NULL),
+    ("quant_out NULL", dict(pattern=6, mutate=_set("quant_out", None)), NULL),
+    ("scale_out NULL", dict(pattern=3, mutate=_set("scale_out", None)), NULL),
+    ("partial_out NULL", dict(pattern=8, P=64, mutate=_set("partial_norm_out", None)), NULL),
+    ("norm_out given to p2", dict(pattern=2, mutate=_set("norm_out", 0x10000)), UNSUPPORTED),
+    ("residual_out given to p0", dict(pattern=0, mutate=_set("residual_out", 0x10000)), UNSUPPORTED),
+    ("quant_out given to p1", dict(pattern=1, mutate=_set("quant_out", 0x10000)), UNSUPPORTED),
+    ("out misaligned", dict(mutate=lambda a, o: o.update(norm_out=o["norm_out"] + 4)), ALIGN),
+    ("scale_out misaligned", dict(pattern=6, mutate=lambda a, o: o.update(scale_out=o["scale_out"] + 2)), ALIGN),
+    ("partial_cols 0", dict(pattern=8, P=0), SHAPE),
+    ("partial_cols > H", dict(pattern=8, P=264), SHAPE),
+    ("partial_cols % 8", dict(pattern=7, P=100), SHAPE),
+    ("sf layout 8x4", dict(pattern=3, sf_layout=1), UNSUPPORTED),
+    ("sf layout 7", dict(pattern=5, sf_layout=7), BAD_PATTERN),
+    ("reserved", dict(mutate=_set("reserved", 1)), UNSUPPORTED),
+    ("outputs overlap", dict(mutate=lambda a, o: o.update(norm_out=o["residual_out"] + 16)), ALIAS),
+    ("output overlaps partial", dict(mutate=lambda a, o: o.update(norm_out=a["partials"][1])), ALIAS),
+    ("allreduce_out inside partial 0", dict(pattern=0, mutate=lambda a, o: o.update(
+        allreduce_out=a["partials"][0] + 256)), ALIAS),
+    ("allreduce_out == partials[1]", dict(pattern=0, mutate=lambda a, o: o.update(
+        allreduce_out=a["partials"][1])), ALIAS),
+    ("norm_out == residual", dict(mutate=lambda a, o: o.update(norm_out=a["residual"])), ALIAS),
+    ("output overlaps gamma", dict(mutate=lambda a, o: o.update(residual_out=a["gamma"])), ALIAS),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", NEG_FUSED, ids=[c[0] for c in NEG_FUSED])
+def test_fused_rejects(lib, name, kw, want):
+    st, detail = _fused_call(lib, **kw)
+    assert st == want, (name, st, detail)
+    assert detail, "a failure must explain itself"
+
+
+def test_in_place_aliases_are_accepted(lib):
+    # allreduce_out == partials[0] and residual_out == residual pass validation
+    # (checked with T = 0 so nothing launches)
+    st, d = _fused_call(lib, pattern=0, T=0, mutate=lambda a, o: o.update(allreduce_out=a["partials"][0]))
+    assert st == TS_OK, d
+    st, d = _fused_call(lib, pattern=1, T=0, mutate=lambda a, o: o.update(residual_out=a["residual"]))
+    assert st == TS_OK, d
+
+
+# ---------------------------------------------------------------------------
+# ts_qk_norm_sharded
+# ---------------------------------------------------------------------------
+
+def _qk_call(lib, R=8, T=4, stride=1280, Q=1024, K=128, ldq=None, ldk=None, mutate=None):
+    f = Fake()
+    a = dict(shards=[f() for _ in range(R)], R=R, T=T, stride=stride, Q=Q, K=K, wq=f(), wk=f(),
+             q_out=f(), ldq=R * Q if ldq is None else ldq, k_out=f(), ldk=R * K if ldk is None else ldk)
+    if mutate:
+        mutate(a)
+    arr = None if a["shards"] is None else (ctypes.c_void_p * len(a["shards"]))(*a["shards"])
+    st = lib.ts_qk_norm_sharded(arr, a["R"], a["T"], a["stride"], a["Q"], a["K"], a["wq"], a["wk"], 1e-6,
+                                a["q_out"], a["ldq"], a["k_out"], a["ldk"], None)
+    return st, lib.ts_last_error_detail().decode()
+
+
+def test_qk_zero_tokens_is_valid(lib):
+    assert _qk_call(lib, T=0)[0] == TS_OK
+
+
+NEG_QK = [
+    ("shards NULL", dict(mutate=lambda a: a.update(shards=None)), NULL),
+    ("R 0", dict(mutate=lambda a: a.update(R=0)), SHAPE),
+    ("R 17", dict(R=17, stride=1280), SHAPE),
+    ("T < 0", dict(T=-5), SHAPE),
+    ("Q % 8", dict(Q=1020), SHAPE),
+    ("K 0", dict(K=0), SHAPE),
+    ("Q too big", dict(Q=4104, stride=8192), UNSUPPORTED),
+    ("K too big", dict(K=1032, stride=8192), UNSUPPORTED),
+    ("stride small", dict(stride=1144), SHAPE),
+    ("stride % 8", dict(stride=1284), SHAPE),
+    ("ldq small", dict(ldq=1024 * 8 - 8), SHAPE),
+    ("ldk % 8", dict(ldk=128 * 8 + 4), SHAPE),
+    ("shard NULL", dict(mutate=lambda a: a["shards"].__setitem__(3, None)), NULL),
+    ("shard misaligned", dict(mutate=lambda a: a["shards"].__setitem__(3, a["shards"][3] + 8)), ALIGN),
+    ("wq NULL", dict(mutate=lambda a: a.update(wq=None)), NULL),
+    ("k_out misaligned", dict(mutate=lambda a: a.update(k_out=a["k_out"] + 2)), ALIGN),
+    ("q_out overlaps k_out", dict(mutate=lambda a: a.update(k_out=a["q_out"] + 64)), ALIAS),
+    ("q_out overlaps a shard", dict(mutate=lambda a: a.update(q_out=a["shards"][2] + 1024)), ALIAS),
+    ("k_out overlaps wk", dict(mutate=lambda a: a.update(k_out=a["wk"])), ALIAS),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", NEG_QK, ids=[c[0] for c in NEG_QK])
+def test_qk_rejects(lib, name, kw, want):
+    st, detail = _qk_call(lib, **kw)
+    assert st == want, (name, st, detail)
+    assert detail
+
+
+def test_binding_requires_cuda_tensors():
+    import torch
+
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        pkg.ts_fused_reduce_norm(0, [x], allreduce_out=x)

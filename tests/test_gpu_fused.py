@@ -1,0 +1,310 @@
+"""GPU parity of ts_fused_reduce_norm against the CPU oracle, through the C ABI.
+
+Tolerances (written here, applied to every case):
+  * allreduce_out, residual_out: bit-exact (fixed fp32 order, no FMA).
+  * norm_out, partial_norm_out: every element within 1 bf16 ulp, >= 99.9 %
+    bit-identical (the GPU's fp32 tree sum of x^2 and rsqrtf differ from the
+    oracle's double sum and correctly rounded rsqrt by a few fp32 ulps).
+  * FP8 / FP4 codes and E4M3 scale factors: bit-exact except where that
+    difference flips a rounding decision: at most 1 code step, on at most
+    1e-4 of the elements; fp32 block scales likewise within one bf16 ulp of
+    amax on at most 1e-3 of the groups.
+  * Exact self-consistency: the oracle's encoders applied to the GPU's own
+    bf16 norm reproduce the GPU's codes and scales bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import reduce_residual_rmsnorm_gb300 as pkg
+from reduce_residual_rmsnorm_gb300 import workloads as wl
+from tests.gpu_util import guarded_outputs, host
+from tests.helpers import (assert_bf16_close, codes_close, e2m1_nibbles, e2m1_order, e4m3_order,
+                           f32_of_bf16, ulp_diff)
+
+pytestmark = pytest.mark.gpu
+
+EPS = 1e-6
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def _inputs(R, T, H, seed, p_std=1.0, outliers=0.0):
+    return wl.fused_inputs(wl.FusedShape(R=R, T=T, H=H, p_std=p_std, outlier_frac=outliers), seed=seed)
+
+
+def _run_gpu(dev, pattern, inp, scale=None, P=0, swizzled=False, allreduce=True, stream=None):
+    parts = inp["partials"].to(dev)
+    res = inp["residual"].to(dev)
+    gamma = inp["gamma"].to(dev)
+    T, H = res.shape
+    g = guarded_outputs(pattern, T, H, dev, P, swizzled, allreduce)
+    sf = None if scale is None else torch.tensor([scale], dtype=torch.float32, device=dev)
+    layout = pkg.SFLayout.SWIZZLED_128x4 if swizzled else pkg.SFLayout.LINEAR
+    pkg.ts_fused_reduce_norm(pattern, parts, None if pattern == 0 else res, None if pattern == 0 else gamma,
+                             EPS, sf, sf_layout=layout, stream=stream, **{k: v.t for k, v in g.items()})
+    torch.cuda.synchronize()
+    for k, v in g.items():
+        assert v.intact(), f"write outside {k}"
+    return {k: host(v.t) for k, v in g.items()}
+
+
+def _oracle(pattern, inp, scale=0.0, P=0, rows=None):
+    return oracle.fused_reduce_norm(pattern, [wl.bits(p) for p in inp["partials"]], wl.bits(inp["residual"]),
+                                    wl.bits(inp["gamma"]), EPS, scale, P, rows=rows)
+
+
+def _compare(pattern, got, want, swizzled=False, T=None, rows=None):
+    """got: full GPU outputs; want: oracle outputs on ``rows`` (all by default)."""
+    sel = (lambda a: a) if rows is None else (lambda a: a[rows])
+    assert np.array_equal(sel(got["allreduce_out"]), want["allreduce_out"]), "allreduce_out"
+    if pattern == 0:
+        return
+    assert np.array_equal(sel(got["residual_out"]), want["residual_out"]), "residual_out"
+    if "norm_out" in got:
+        assert_bf16_close(sel(got["norm_out"]), want["norm_out"], 1, 0.999, "norm_out")
+    if "partial_norm_out" in got:
+        assert_bf16_close(sel(got["partial_norm_out"]), want["partial_norm_out"], 1, 0.999, "partial_norm_out")
+    if pattern in (2, 4, 6, 7):
+        codes_close(sel(got["quant_out"]), want["quant_out"], e4m3_order, 1, 1e-4, "e4m3 codes")
+    if pattern in (6, 7):
+        gs, ws = sel(got["scale_out"]), want["block_scale_out"]
+        diff = gs != ws
+        assert diff.mean() <= 1e-3, f"{diff.mean():.2e} of block scales differ"
+        assert (np.abs(gs - ws) <= np.abs(ws) * 2.0 ** -7).all()
+    if pattern in (3, 5):
+        codes_close(e2m1_nibbles(sel(got["quant_out"])), e2m1_nibbles(want["quant_out"]), e2m1_order, 1,
+                    1e-4, "e2m1 codes")
+        sf = got["scale_out"]
+        if swizzled:
+            lin = np.zeros_like(want["sf_out"])
+            full_rows = np.arange(T) if rows is None else rows
+            n_sf = want["sf_out"].shape[1]
+            flat = sf.reshape(-1)
+            for i, m in enumerate(full_rows):
+                offs = [oracle.sf_offset_swizzled_128x4(int(m), k, n_sf) for k in range(n_sf)]
+                lin[i] = flat[offs]
+            codes_close(lin, want["sf_out"], e4m3_order, 1, 1e-4, "SF (swizzled)")
+        else:
+            codes_close(sel(sf), want["sf_out"], e4m3_order, 1, 1e-4, "SF (linear)")
+
+
+def _self_consistency(pattern, got, scale):
+    """Oracle encoders on the GPU's own n reproduce the GPU's codes exactly."""
+    n = f32_of_bf16(got["norm_ref"])
+    T, H = n.shape
+    if pattern in (2, 4):
+        want = oracle.e4m3_encode(n * np.float32(scale))
+        assert np.array_equal(got["quant_out"], want)
+    elif pattern in (6, 7):
+        g = n.reshape(T, H // 128, 128)
+        s = np.abs(g).max(-1).astype(np.float32) / np.float32(448.0)
+        assert np.array_equal(got["scale_out"], s)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            q = oracle.e4m3_encode((g / s[..., None]).astype(np.float32)).reshape(T, H)
+        q[np.repeat(s == 0, 128, axis=-1).reshape(T, H)] = 0
+        assert np.array_equal(got["quant_out"], q)
+    elif pattern in (3, 5):
+        g = n.reshape(T, H // 16, 16)
+        amax = np.abs(g).max(-1).astype(np.float32)
+        sf = oracle.e4m3_encode(np.float32(scale) * (amax / np.float32(6.0)))
+        d = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))[sf]
+        with np.errstate(divide="ignore", invalid="ignore"):
+            es = np.where(d == 0, np.float32(0), np.float32(scale) / d).astype(np.float32)
+        codes = oracle.e2m1_encode((g * es[..., None]).astype(np.float32)).reshape(T, H)
+        codes[np.repeat(d == 0, 16, axis=-1).reshape(T, H)] = 0
+        packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+        assert np.array_equal(got["quant_out"], packed)
+        return sf
+    return None
+
+
+# ---------------------------------------------------------------------------
+# small and ragged shapes: every row through the oracle
+# ---------------------------------------------------------------------------
+
+SHAPES = [  # (R, T, H)
+    (2, 16, 4096),   # the kARResidualRMSNorm R=2 workload
+    (1, 1, 8),
+    (3, 5, 136),
+    (8, 37, 7168),
+    (16, 9, 1024),
+    (5, 130, 5120),
+    (4, 3, 16384),
+    (7, 64, 2112),
+]
+
+
+def _ok_for(pattern, H):
+    if pattern in (6, 7):
+        return H % 128 == 0
+    if pattern in (3, 5):
+        return H % 16 == 0
+    return True
+
+
+@pytest.mark.parametrize("R,T,H", SHAPES, ids=[f"R{r}-T{t}-H{h}" for r, t, h in SHAPES])
+@pytest.mark.parametrize("pattern", list(range(9)))
+def test_small_shapes(dev, pattern, R, T, H):
+    if not _ok_for(pattern, H):
+        pytest.skip("H not a multiple of the quantisation group")
+    inp = _inputs(R, T, H, seed=R * 1000 + T + H)
+    P = min(H, 1024) // 8 * 8 if pattern in (7, 8) else 0
+    base = _run_gpu(dev, 1, inp)
+    amax = float(np.abs(f32_of_bf16(base["norm_out"])).max())
+    scale = {2: 448.0 / amax, 4: 448.0 / amax, 3: 2688.0 / amax, 5: 2688.0 / amax}.get(pattern)
+    for swz in ((False, True) if pattern in (3, 5) else (False,)):
+        got = _run_gpu(dev, pattern, inp, scale, P, swz)
+        want = _oracle(pattern, inp, scale or 0.0, P)
+        _compare(pattern, got, want, swz, T)
+        if pattern in (2, 3, 4, 5, 6, 7):
+            got["norm_ref"] = base["norm_out"]
+            sf = _self_consistency(pattern, got, scale)
+            if swz:
+                assert np.array_equal(got["scale_out"].reshape(-1), oracle.sf_swizzle_128x4(sf))
+
+
+def test_zero_rows(dev):
+    """All-zero inputs: norm 0, block scale 0 with codes 0, SF 0 with codes 0."""
+    R, T, H = 2, 3, 256
+    z = torch.zeros((R, T, H), dtype=torch.bfloat16)
+    inp = {"partials": z, "residual": torch.zeros((T, H), dtype=torch.bfloat16),
+           "gamma": torch.ones(H, dtype=torch.bfloat16)}
+    for pattern, scale in ((1, None), (2, 10.0), (3, 100.0), (6, None), (8, None)):
+        got = _run_gpu(dev, pattern, inp, scale, 64 if pattern == 8 else 0)
+        _compare(pattern, got, _oracle(pattern, inp, scale or 0.0, 64 if pattern == 8 else 0), T=T)
+        for k, v in got.items():
+            assert (v == 0).all(), (pattern, k)
+
+
+def test_saturation_and_extremes(dev):
+    R, T, H = 4, 8, 512
+    inp = _inputs(R, T, H, seed=7, p_std=3.0e4)  # large values: x^2 ~ 1e10 per element
+    got = _run_gpu(dev, 2, inp, scale=1.0e4)  # most codes saturate to +-448
+    want = _oracle(2, inp, 1.0e4)
+    _compare(2, got, want, T=T)
+    assert ((got["quant_out"] & 0x7F) == 0x7E).mean() > 0.5
+    got = _run_gpu(dev, 3, inp, scale=1.0e6)  # SFs saturate to 448
+    _compare(3, got, _oracle(3, inp, 1.0e6), T=T)
+
+
+def test_in_place_allreduce_and_residual(dev):
+    R, T, H = 4, 33, 1024
+    inp = _inputs(R, T, H, seed=8)
+    want = _oracle(1, inp)
+    parts = inp["partials"].to(dev).clone()
+    res = inp["residual"].to(dev).clone()
+    gamma = inp["gamma"].to(dev)
+    norm = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    pkg.ts_fused_reduce_norm(1, parts, res, gamma, EPS, allreduce_out=parts[0], residual_out=res, norm_out=norm)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(parts[0]), want["allreduce_out"])
+    assert np.array_equal(host(res), want["residual_out"])
+    assert_bf16_close(host(norm), want["norm_out"], 1, 0.999, "in-place norm")
+    parts2 = inp["partials"].to(dev).clone()
+    pkg.ts_fused_reduce_norm(0, parts2, allreduce_out=parts2[0])
+    torch.cuda.synchronize()
+    assert np.array_equal(host(parts2[0]), want["allreduce_out"])
+
+
+def test_side_stream_and_zero_tokens(dev):
+    inp = _inputs(2, 16, 4096, seed=9)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        got = _run_gpu(dev, 1, inp, stream=s)
+    _compare(1, got, _oracle(1, inp), T=16)
+    empty = torch.empty((2, 0, 4096), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((0, 4096), dtype=torch.bfloat16, device=dev)
+    pkg.ts_fused_reduce_norm(1, empty, out, torch.ones(4096, dtype=torch.bfloat16, device=dev), EPS,
+                             residual_out=torch.empty_like(out), norm_out=torch.empty_like(out))
+
+
+def test_deterministic(dev):
+    inp = _inputs(8, 64, 7168, seed=10)
+    a = _run_gpu(dev, 6, inp)
+    b = _run_gpu(dev, 6, inp)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: sampled rows through the oracle, exact self-consistency
+# on every row
+# ---------------------------------------------------------------------------
+
+def _sample_rows(T, n=192, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([np.arange(min(32, T)), np.arange(max(0, T - 32), T),
+                                     rng.integers(0, T, n)]))
+    return rows
+
+
+@pytest.mark.slow
+def test_full_size_allreduce_rmsnorm(dev):
+    """kARResidualRMSNorm and kAllReduce, R=8, T=4096, H=7168: every row."""
+    inp = wl.fused_inputs(wl.WORKLOADS["C2"], seed=0)
+    for pattern in (1, 0):
+        got = _run_gpu(dev, pattern, inp, allreduce=True)
+        _compare(pattern, got, _oracle(pattern, inp))
+
+
+@pytest.mark.slow
+def test_full_size_fp8(dev):
+    """FP8 per-tensor, FP8 1x128 blockwise, PartialOut (+FP8 blockwise), R=8,
+    T=8192, H=7168 with 0.1 % outliers x50."""
+    inp = wl.fused_inputs(wl.WORKLOADS["C3"], seed=0)
+    base = _run_gpu(dev, 1, inp, allreduce=False)
+    amax = float(np.abs(f32_of_bf16(base["norm_out"])).max())
+    rows = _sample_rows(8192)
+    sigma = float(np.float32(448.0) / np.float32(amax))
+    for pattern, scale, P in ((2, sigma, 0), (6, None, 0), (7, None, 1024), (8, None, 1024)):
+        got = _run_gpu(dev, pattern, inp, scale, P, allreduce=False)
+        want = _oracle(pattern, inp, scale or 0.0, P, rows=rows)
+        _compare_rows(pattern, got, want, rows)
+        if pattern in (2, 6, 7):
+            got["norm_ref"] = base["norm_out"]
+            _self_consistency(pattern, got, scale)
+        if pattern == 8:
+            assert np.array_equal(got["partial_norm_out"], base["norm_out"][:, :1024])
+
+
+def _compare_rows(pattern, got, want, rows):
+    assert np.array_equal(got["residual_out"][rows], want["residual_out"]), "residual_out"
+    w = want
+    if "partial_norm_out" in got:
+        assert_bf16_close(got["partial_norm_out"][rows], want["partial_norm_out"], 1, 0.999, "partial")
+    if pattern in (2, 4, 6, 7):
+        codes_close(got["quant_out"][rows], w["quant_out"], e4m3_order, 1, 1e-4, "e4m3 codes")
+    if pattern in (6, 7):
+        gs, ws = got["scale_out"][rows], w["block_scale_out"]
+        assert (gs != ws).mean() <= 1e-3
+        assert (np.abs(gs - ws) <= np.abs(ws) * 2.0 ** -7).all()
+
+
+@pytest.mark.slow
+def test_full_size_nvfp4(dev):
+    """NVFP4, R=4, T=16384, H=5120, SF in LINEAR and SWIZZLED_128x4."""
+    inp = wl.fused_inputs(wl.WORKLOADS["C4"], seed=0)
+    base = _run_gpu(dev, 1, inp, allreduce=False)
+    amax = float(np.abs(f32_of_bf16(base["norm_out"])).max())
+    g = float(np.float32(2688.0) / np.float32(amax))
+    rows = _sample_rows(16384)
+    want = _oracle(3, inp, g, rows=rows)
+    lin = _run_gpu(dev, 3, inp, g, allreduce=False)
+    assert np.array_equal(lin["residual_out"][rows], want["residual_out"])
+    codes_close(e2m1_nibbles(lin["quant_out"][rows]), e2m1_nibbles(want["quant_out"]), e2m1_order, 1, 1e-4,
+                "e2m1")
+    codes_close(lin["scale_out"][rows], want["sf_out"], e4m3_order, 1, 1e-4, "SF")
+    lin["norm_ref"] = base["norm_out"]
+    sf = _self_consistency(3, lin, g)
+    swz = _run_gpu(dev, 3, inp, g, swizzled=True, allreduce=False)
+    assert np.array_equal(swz["quant_out"], lin["quant_out"])
+    assert np.array_equal(swz["scale_out"].reshape(-1), oracle.sf_swizzle_128x4(sf))
