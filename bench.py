@@ -89,11 +89,15 @@ def read_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ("fused_rows.cu", "qk_norm.cu", "device_util.cuh", "launch.h")
+
+
 def kernel_source_hash() -> str:
+    """Hash of the device-code sources (not the host-side argument checks)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "reduce_residual_rmsnorm_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
+        if fn in KERNEL_SOURCES:
             with open(os.path.join(csrc, fn), "rb") as f:
                 h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]

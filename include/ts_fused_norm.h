@@ -156,7 +156,9 @@ typedef struct {
  *                 code = e4m3(n * sigma)) or the NVFP4 global scale g (patterns
  *                 3, 5); required for 2..5, ignored otherwise.  A device pointer
  *                 so the call can be captured in a CUDA graph.
- *   T             rows (tokens), >= 0.  T == 0 validates and returns TS_OK.
+ *   T             rows (tokens), >= 0.  T == 0 validates and returns TS_OK
+ *                 without launching; the per-row buffers (partials, residual,
+ *                 outputs) may then be NULL, as empty tensors are.
  *   H             hidden size: multiple of 8, <= 16384; multiple of 128 for
  *                 patterns 6, 7; multiple of 16 for patterns 3, 5.
  *   outs          host pointer to the output set (see ts_outs_t).
@@ -180,7 +182,8 @@ TS_API int ts_fused_reduce_norm(int pattern, const void *const *partials, int R,
  *   qkv_shards    host array of R device pointers; shard r is bf16 [T, row_stride]
  *                 holding q (Q columns) | k (K columns) | v (not read).
  *   R             1..16.
- *   T             tokens, >= 0 (T == 0 returns TS_OK).
+ *   T             tokens, >= 0 (T == 0 returns TS_OK without launching; the
+ *                 shards and outputs may then be NULL).
  *   row_stride    elements between consecutive tokens of a shard; multiple of 8,
  *                 >= Q + K.
  *   q_shard (Q)   8 <= Q <= 4096, multiple of 8.   k_shard (K): 8 <= K <= 1024,

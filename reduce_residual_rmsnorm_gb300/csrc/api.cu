@@ -120,15 +120,16 @@ extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, in
     if (outs->reserved != 0)
         return fail(TS_ERR_UNSUPPORTED, "ts_outs_t.reserved must be 0");
 
-    // inputs
+    // inputs (with T == 0 the per-row buffers may be NULL: empty tensors)
+    const bool empty = T == 0;
     for (int r = 0; r < R; ++r) {
-        if (partials[r] == nullptr)
+        if (partials[r] == nullptr && !empty)
             return fail(TS_ERR_NULL, "partials[%d] is NULL", r);
         if (!aligned(partials[r], 16))
             return fail(TS_ERR_ALIGN, "partials[%d] is not 16-byte aligned", r);
     }
     if (pattern != 0) {
-        if (residual == nullptr)
+        if (residual == nullptr && !empty)
             return fail(TS_ERR_NULL, "residual is NULL (required for pattern %d)", pattern);
         if (gamma == nullptr)
             return fail(TS_ERR_NULL, "gamma is NULL (required for pattern %d)", pattern);
@@ -150,7 +151,7 @@ extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, in
                               outs->partial_norm_out, outs->quant_out, outs->scale_out};
     const char *row = kOutputTable[pattern];
     for (int i = 0; i < 6; ++i) {
-        if (row[i] == 'R' && out_ptr[i] == nullptr)
+        if (row[i] == 'R' && out_ptr[i] == nullptr && !empty)
             return fail(TS_ERR_NULL, "%s is required for pattern %d", kOutputNames[i], pattern);
         if (row[i] == '-' && out_ptr[i] != nullptr)
             return fail(TS_ERR_UNSUPPORTED, "%s is not an output of pattern %d (pass NULL)",
@@ -280,8 +281,9 @@ extern "C" int ts_qk_norm_sharded(const void *const *qkv_shards, int R, int64_t 
         return fail(TS_ERR_SHAPE, "ldq = %lld must be a multiple of 8 and >= R*q_shard", (long long)ldq);
     if (ldk % 8 != 0 || ldk < R * k_shard)
         return fail(TS_ERR_SHAPE, "ldk = %lld must be a multiple of 8 and >= R*k_shard", (long long)ldk);
+    const bool empty = T == 0;  // per-token buffers may then be NULL (empty tensors)
     for (int r = 0; r < R; ++r) {
-        if (qkv_shards[r] == nullptr)
+        if (qkv_shards[r] == nullptr && !empty)
             return fail(TS_ERR_NULL, "qkv_shards[%d] is NULL", r);
         if (!aligned(qkv_shards[r], 16))
             return fail(TS_ERR_ALIGN, "qkv_shards[%d] is not 16-byte aligned", r);
@@ -289,7 +291,7 @@ extern "C" int ts_qk_norm_sharded(const void *const *qkv_shards, int R, int64_t 
     const void *const ptrs[4] = {q_weight, k_weight, q_out, k_out};
     const char *const names[4] = {"q_weight", "k_weight", "q_out", "k_out"};
     for (int i = 0; i < 4; ++i) {
-        if (ptrs[i] == nullptr)
+        if (ptrs[i] == nullptr && !(empty && i >= 2))
             return fail(TS_ERR_NULL, "%s is NULL", names[i]);
         if (!aligned(ptrs[i], 16))
             return fail(TS_ERR_ALIGN, "%s is not 16-byte aligned", names[i]);

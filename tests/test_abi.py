@@ -163,6 +163,22 @@ def test_fused_rejects(lib, name, kw, want):
     assert detail, "a failure must explain itself"
 
 
+def test_zero_rows_accepts_null_row_buffers(lib):
+    def nullify(a, o):
+        a["partials"] = [None] * len(a["partials"])
+        a["residual"] = None
+        for k in ("allreduce_out", "residual_out", "norm_out", "quant_out", "scale_out"):
+            o[k] = None
+    st, d = _fused_call(lib, pattern=1, T=0, mutate=nullify)
+    assert st == TS_OK, d
+    st, d = _fused_call(lib, pattern=1, T=1, mutate=nullify)
+    assert st == NULL, d
+    st, d = _qk_call(lib, T=0, mutate=lambda a: a.update(shards=[None] * 8, q_out=None, k_out=None))
+    assert st == TS_OK, d
+    st, d = _qk_call(lib, T=0, mutate=lambda a: a.update(wq=None))
+    assert st == NULL, d
+
+
 def test_in_place_aliases_are_accepted(lib):
     # allreduce_out == partials[0] and residual_out == residual pass validation
     # (checked with T = 0 so nothing launches)
