@@ -99,6 +99,10 @@ def load(path: str | None = None):
             ctypes.c_int64, c_u16p, c_u16p, ctypes.c_float, c_i64p, ctypes.c_int64,
             c_u16p, c_u16p]
         lib.orc_qk_norm_sharded_rows.restype = ctypes.c_int
+        lib.orc_rms_norm_sharded_rows.argtypes = [
+            ctypes.c_int, ctypes.POINTER(c_u16p), ctypes.c_int64, ctypes.c_int64, c_u16p,
+            ctypes.c_float, c_i64p, ctypes.c_int64, c_u16p]
+        lib.orc_rms_norm_sharded_rows.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -265,3 +269,28 @@ def qk_norm_sharded(shards, q_shard: int, k_shard: int, q_weight, k_weight, eps:
     if rc != 0:
         raise ValueError("oracle rejected the QK arguments")
     return q_out, k_out
+
+
+def rms_norm_sharded(shards, width: int, weight, eps: float = 1e-6, rows=None) -> np.ndarray:
+    """Single-matrix sharded RMSNorm on the listed tokens.
+
+    ``shards``: R uint16 arrays [T, row_stride] (the first ``width`` columns are
+    the shard's slice of the hidden dim); ``weight``: uint16 [R*width].
+    Returns uint16 [n, R*width] (shard r at columns r*width...).
+    """
+    sh = [_u16(s) for s in shards]
+    R = len(sh)
+    T, stride = sh[0].shape
+    for s in sh:
+        assert s.shape == (T, stride)
+    w = _u16(weight)
+    assert w.shape == (R * width,)
+    rows = np.arange(T, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, R * width), np.uint16)
+    arr = (ctypes.POINTER(ctypes.c_uint16) * R)(*[_ptr(s, ctypes.c_uint16) for s in sh])
+    rc = load().orc_rms_norm_sharded_rows(R, arr, stride, width, _ptr(w, ctypes.c_uint16), float(eps),
+                                          _ptr(rows, ctypes.c_int64), rows.size,
+                                          _ptr(out, ctypes.c_uint16))
+    if rc != 0:
+        raise ValueError("oracle rejected the sharded RMSNorm arguments")
+    return out

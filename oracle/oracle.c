@@ -468,3 +468,45 @@ int orc_qk_norm_sharded_rows(int R, const uint16_t *const *shards, int64_t row_s
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Single-matrix sharded RMSNorm ([P1] `minimax_allreduce_rms`: all-reduce  */
+/* of the per-token variance of a hidden dim split over R ranks, then       */
+/* RMSNorm of each rank's slice with its slice of the weight).              */
+/* ------------------------------------------------------------------------ */
+
+/* For every listed token t and every shard r (W values at stride row_stride):
+ *   v_r = mean over j < W of float32(x_r[t,j])^2   (double sum, rounded once)
+ *   V   = sum over r ascending of v_r, fp32
+ *   out[t, r*W + j] = bf16((x_r[t,j] * rsqrt(V/R + eps)) * weight[r*W + j])
+ * The same steps as the QK norm above, for one segment.  Outputs are
+ * compact [nrows, R*W].  Returns 0 or -1. */
+int orc_rms_norm_sharded_rows(int R, const uint16_t *const *shards, int64_t row_stride, int64_t W,
+                              const uint16_t *weight, float eps, const int64_t *rows, int64_t nrows,
+                              uint16_t *out)
+{
+    if (R < 1 || W < 1 || row_stride < W)
+        return -1;
+    for (int64_t ri = 0; ri < nrows; ++ri) {
+        const int64_t t = rows[ri];
+        float V = 0.0f;
+        for (int r = 0; r < R; ++r) {
+            const uint16_t *base = shards[r] + t * row_stride;
+            double s = 0.0;
+            for (int64_t j = 0; j < W; ++j) {
+                double v = orc_bf16_decode(base[j]);
+                s += v * v;
+            }
+            V = V + (float)(s / (double)W);
+        }
+        float inv = (float)(1.0 / sqrt((double)(V / (float)R + eps)));
+        for (int r = 0; r < R; ++r) {
+            const uint16_t *base = shards[r] + t * row_stride;
+            for (int64_t j = 0; j < W; ++j) {
+                float y = (orc_bf16_decode(base[j]) * inv) * orc_bf16_decode(weight[r * W + j]);
+                out[ri * R * W + r * W + j] = orc_bf16_encode(y);
+            }
+        }
+    }
+    return 0;
+}

@@ -146,3 +146,51 @@ def test_agrees_with_eager_torch_definition(orc):
     to_bits = lambda x: x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)  # noqa: E731
     assert_bf16_close(q_out, to_bits(q_ref), 1, 0.99, "eager q")
     assert_bf16_close(k_out, to_bits(k_ref), 1, 0.99, "eager k")
+
+
+# ---------------------------------------------------------------------------
+# single-matrix sharded RMSNorm (one segment instead of q and k)
+# ---------------------------------------------------------------------------
+
+def test_single_matrix_equals_unsharded_rmsnorm(orc):
+    rng = np.random.default_rng(40)
+    R, T, W = 8, 10, 96
+    shards = [bf16_bits_of_f32(rng.standard_normal((T, W + 16)).astype(np.float32)) for _ in range(R)]
+    w = bf16_bits_of_f32(rng.uniform(0.5, 1.5, R * W).astype(np.float32))
+    out = orc.rms_norm_sharded(shards, W, w, eps=EPS)
+    cat = np.concatenate([s[:, :W] for s in shards], axis=1)
+    want = orc.fused_reduce_norm(1, [cat], np.zeros_like(cat), w, eps=EPS)["norm_out"]
+    assert_bf16_close(out, want, 1, 0.99, "single-matrix vs unsharded")
+
+
+def test_single_matrix_is_the_q_segment_of_qk(orc):
+    """With the same shards, the single-matrix norm of the first W columns is
+    the QK norm's q output (the k segment does not enter q's variance)."""
+    rng = np.random.default_rng(41)
+    R, T, Q, K = 3, 7, 64, 16
+    shards, wq, wk = _qk_inputs(rng, R, T, Q, K, 8)
+    q_out, _ = orc.qk_norm_sharded(shards, Q, K, wq, wk, eps=EPS)
+    assert np.array_equal(orc.rms_norm_sharded(shards, Q, wq, eps=EPS), q_out)
+
+
+def test_single_matrix_single_shard_textbook(orc):
+    rng = np.random.default_rng(42)
+    T, W = 5, 256
+    sh = [bf16_bits_of_f32(rng.standard_normal((T, W)).astype(np.float32) * 3)]
+    w = bf16_bits_of_f32(rng.uniform(0.5, 1.5, W).astype(np.float32))
+    out = orc.rms_norm_sharded(sh, W, w, eps=EPS)
+    x = f32_of_bf16(sh[0]).astype(np.float64)
+    want = x / np.sqrt((x * x).mean(1, keepdims=True) + EPS) * f32_of_bf16(w)
+    assert_bf16_close(out, bf16_of_f64(want), 1, 0.99, "single shard")
+
+
+def test_single_matrix_constant_rows(orc):
+    R, T, W = 4, 2, 32
+    cs = [0.75, -0.5, 2.0 ** -11, 3.0]
+    sh = [bf16_bits_of_f32(np.full((T, W), c, np.float32)) for c in cs]
+    rng = np.random.default_rng(43)
+    w = bf16_bits_of_f32(rng.uniform(0.5, 1.5, R * W).astype(np.float32))
+    out = orc.rms_norm_sharded(sh, W, w, eps=EPS)
+    ms = float(np.mean(np.square(cs)))
+    want = bf16_of_f64(f32_of_bf16(w).astype(np.float64) * np.repeat(cs, W) / np.sqrt(ms + EPS))
+    assert_bf16_close(out, np.broadcast_to(want, out.shape), 1, 0.99, "constant")
