@@ -89,6 +89,12 @@ def load(path: str | None = None):
         lib.orc_sf_offset_swizzled_128x4.restype = ctypes.c_int64
         lib.orc_sf_swizzle_128x4.argtypes = [c_u8p, ctypes.c_int64, ctypes.c_int64, c_u8p]
         lib.orc_sf_swizzle_128x4.restype = None
+        lib.orc_sf_swizzled8_rows.argtypes = [ctypes.c_int64]
+        lib.orc_sf_swizzled8_rows.restype = ctypes.c_int64
+        lib.orc_sf_offset_swizzled_8x4.argtypes = [ctypes.c_int64] * 3
+        lib.orc_sf_offset_swizzled_8x4.restype = ctypes.c_int64
+        lib.orc_sf_swizzle_8x4.argtypes = [c_u8p, ctypes.c_int64, ctypes.c_int64, c_u8p]
+        lib.orc_sf_swizzle_8x4.restype = None
         lib.orc_fused_reduce_norm_rows.argtypes = [
             ctypes.c_int, ctypes.c_int, ctypes.POINTER(c_u16p), c_u16p, c_u16p,
             ctypes.c_float, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
@@ -186,8 +192,26 @@ def sf_swizzle_128x4(linear: np.ndarray) -> np.ndarray:
     return out
 
 
+def sf_swizzled8_shape(rows: int, n_sf_cols: int) -> tuple[int, int]:
+    lib = load()
+    return int(lib.orc_sf_swizzled8_rows(rows)), int(lib.orc_sf_swizzled_cols(n_sf_cols))
+
+
+def sf_offset_swizzled_8x4(m: int, k: int, n_sf_cols: int) -> int:
+    return int(load().orc_sf_offset_swizzled_8x4(m, k, n_sf_cols))
+
+
+def sf_swizzle_8x4(linear: np.ndarray) -> np.ndarray:
+    linear = np.ascontiguousarray(linear, dtype=np.uint8)
+    rows, cols = linear.shape
+    pr, pc = sf_swizzled8_shape(rows, cols)
+    out = np.empty(pr * pc, np.uint8)
+    load().orc_sf_swizzle_8x4(_ptr(linear, ctypes.c_uint8), rows, cols, _ptr(out, ctypes.c_uint8))
+    return out
+
+
 # --------------------------------------------------------------------------
-# the two operations
+# the operations
 # --------------------------------------------------------------------------
 
 def fused_reduce_norm(pattern: int, partials, residual=None, gamma=None, eps: float = 1e-6,

@@ -41,6 +41,7 @@
  *   c12 E2M1 grid {0,.5,1,1.5,2,3,4,6}: nearest, ties to even code, saturate 6.
  *   c13 two E2M1 codes per byte, even element in the low nibble.
  *   c14 SWIZZLED_128x4 scale-factor tile map (see orc_sf_offset_swizzled_128x4).
+ *   c21 SWIZZLED_8x4 scale-factor tile map (see orc_sf_offset_swizzled_8x4).
  *   c15 partial_norm_out holds the first P columns of n; the RMS is over all H.
  *   c18 QK: rsqrt(V / R + eps), V the fp32 shard-ascending sum of shard means.
  */
@@ -242,6 +243,30 @@ int64_t orc_sf_offset_swizzled_128x4(int64_t m, int64_t k, int64_t n_sf_cols)
     int64_t i = (m % 128) / 32;
     int64_t j = m % 32;
     return tile * 512 + j * 16 + i * 4 + (k % 4);
+}
+
+/* Rows of the SWIZZLED_8x4 buffer: rows padded up to a multiple of 8. */
+int64_t orc_sf_swizzled8_rows(int64_t rows) { return (rows + 7) / 8 * 8; }
+
+/* Byte offset of scale factor (m, k) in the SWIZZLED_8x4 layout (the pages
+ * only name it; reading c21): a row-major grid of 8-row x 4-column tiles of 32
+ * bytes, row-major inside a tile (row m%8 at byte 4*(m%8), column k%4 next). */
+int64_t orc_sf_offset_swizzled_8x4(int64_t m, int64_t k, int64_t n_sf_cols)
+{
+    int64_t tiles_per_row = orc_sf_swizzled_cols(n_sf_cols) / 4;
+    int64_t tile = (m / 8) * tiles_per_row + (k / 4);
+    return tile * 32 + (m % 8) * 4 + (k % 4);
+}
+
+/* Scatter a LINEAR [rows, n_sf_cols] matrix into the padded SWIZZLED_8x4
+ * buffer; padding bytes are 0. */
+void orc_sf_swizzle_8x4(const uint8_t *linear, int64_t rows, int64_t n_sf_cols, uint8_t *out)
+{
+    int64_t size = orc_sf_swizzled8_rows(rows) * orc_sf_swizzled_cols(n_sf_cols);
+    memset(out, 0, (size_t)size);
+    for (int64_t m = 0; m < rows; ++m)
+        for (int64_t k = 0; k < n_sf_cols; ++k)
+            out[orc_sf_offset_swizzled_8x4(m, k, n_sf_cols)] = linear[m * n_sf_cols + k];
 }
 
 /* Scatter a LINEAR [rows, n_sf_cols] scale-factor matrix into the padded

@@ -216,3 +216,41 @@ def test_swizzle_pads_with_zero(orc):
             assert out[o] == lin[m, k]
             seen[o] = True
     assert (out[~seen] == 0).all()
+
+
+# --------------------------------------------------------------------------
+# SWIZZLED_8x4 (named on the pages, never defined: the 8-row x 4-column tile
+# reading; its definition stays unpinned by the pages)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,cols", [(1, 1), (3, 5), (8, 4), (9, 9), (37, 320 // 8), (130, 13)])
+def test_swizzle8_is_injective_into_padded_buffer(orc, rows, cols):
+    pr, pc = orc.sf_swizzled8_shape(rows, cols)
+    assert pr % 8 == 0 and pc % 4 == 0 and pr >= rows and pc >= cols and pr - rows < 8
+    offs = np.array([orc.sf_offset_swizzled_8x4(m, k, cols) for m in range(pr) for k in range(pc)])
+    assert offs.min() == 0 and offs.max() == pr * pc - 1
+    assert len(np.unique(offs)) == pr * pc
+
+
+def test_swizzle8_tile_structure(orc):
+    cols = 12  # 3 tiles of 4 columns per 8-row band
+    off = lambda m, k: orc.sf_offset_swizzled_8x4(m, k, cols)  # noqa: E731
+    assert [off(0, k) for k in range(4)] == [0, 1, 2, 3]
+    assert off(1, 0) == 4 and off(7, 3) == 31
+    assert off(0, 4) == 32 and off(0, 8) == 64
+    assert off(8, 0) == 3 * 32
+
+
+def test_swizzle8_pads_with_zero(orc):
+    rng = np.random.default_rng(7)
+    lin = rng.integers(1, 256, size=(11, 6), dtype=np.uint8)
+    out = orc.sf_swizzle_8x4(lin)
+    pr, pc = orc.sf_swizzled8_shape(11, 6)
+    assert out.size == pr * pc == 16 * 8
+    seen = np.zeros(out.size, bool)
+    for m in range(11):
+        for k in range(6):
+            o = orc.sf_offset_swizzled_8x4(m, k, 6)
+            assert out[o] == lin[m, k]
+            seen[o] = True
+    assert (out[~seen] == 0).all()

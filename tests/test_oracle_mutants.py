@@ -38,6 +38,7 @@ MUTANTS = {
     "qk_k_uses_q_mean": ("(double)(Vk / (float)R + eps)", "(double)(Vq / (float)R + eps)"),
     "single_matrix_no_div_r": ("(double)(V / (float)R + eps)", "(double)(V + eps)"),
     "single_matrix_weight_slice": ("orc_bf16_decode(weight[r * W + j])", "orc_bf16_decode(weight[j])"),
+    "swizzle8_row_stride": ("return tile * 32 + (m % 8) * 4 + (k % 4);", "return tile * 32 + (m % 8) * 3 + (k % 4);"),
     "swizzle_rows_cols": ("return tile * 512 + j * 16 + i * 4 + (k % 4);",
                           "return tile * 512 + i * 16 + j * 4 + (k % 4);"),
 }
