@@ -2,7 +2,10 @@
 
 One step = one ``ts_fused_reduce_norm(kARResidualRMSNorm)`` call over the
 R=8, T=4096, H=7168 bf16 workload (partials N(0, 0.5^2), residual N(0, 1),
-gamma U(0.5, 1.5), seed 0), inputs resident in HBM.  Prints one JSON line.
+gamma U(0.5, 1.5), seed 0), inputs resident in HBM, launched with the
+pages' ``launch_with_pdl`` option (programmatic dependent launch: each call
+still waits for the previous one to complete before touching memory).
+Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -47,7 +50,7 @@ L2_BYTES = 129 * 10 ** 6
 # algorithmic bytes (reads of R partials + residual, gamma once, all outputs)
 # ---------------------------------------------------------------------------
 
-def fused_bytes(pattern: int, R: int, T: int, H: int, P: int = 0, swizzled: bool = False,
+def fused_bytes(pattern: int, R: int, T: int, H: int, P: int = 0, sf_layout: int = 2,
                 allreduce_out: bool = False) -> int:
     p = int(pattern)
     rb = T * R * H * 2
@@ -69,12 +72,20 @@ def fused_bytes(pattern: int, R: int, T: int, H: int, P: int = 0, swizzled: bool
         wb += T * (H // 128) * 4
     if p in (3, 5):
         wb += T * H // 2
-        wb += ((T + 127) // 128 * 128) * ((H // 16 + 3) // 4 * 4) if swizzled else T * (H // 16)
+        if sf_layout == 2:  # LINEAR
+            wb += T * (H // 16)
+        else:               # SWIZZLED_128x4 / SWIZZLED_8x4, padding included
+            tile = 128 if sf_layout == 0 else 8
+            wb += ((T + tile - 1) // tile * tile) * ((H // 16 + 3) // 4 * 4)
     return rb + wb
 
 
 def qk_bytes(R: int, T: int, Q: int, K: int) -> int:
     return T * R * (Q + K) * 2 * 2 + R * (Q + K) * 2
+
+
+def rms_sharded_bytes(R: int, T: int, W: int) -> int:
+    return T * R * W * 2 * 2 + R * W * 2
 
 
 # ---------------------------------------------------------------------------
@@ -89,7 +100,7 @@ def read_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = ("fused_rows.cu", "qk_norm.cu", "device_util.cuh", "launch.h")
+KERNEL_SOURCES = ("fused_rows.cu", "qk_norm.cu", "device_util.cuh", "launch.h", "sf_layout.cuh")
 
 
 def kernel_source_hash() -> str:
@@ -111,9 +122,7 @@ def recorded_traffic(key: str):
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("kernel_source_hash") != kernel_source_hash():
-        return None
-    v = rec.get("bytes_per_launch", {}).get(key)
+    v = rec.get("captures", {}).get(kernel_source_hash(), {}).get("bytes_per_launch", {}).get(key)
     return None if v is None else int(v)
 
 
@@ -299,104 +308,151 @@ def roofline_entry(nbytes: int, ms: float, peak: float) -> dict:
     return {"us": ms * 1e3, "bytes": nbytes, "gbs": gbs, "frac": gbs / peak}
 
 
-def measure_rows(dev, stream, peak: float, iters: int) -> dict:
+def _case_builders():
+    """name -> builder(dev, stream) returning (call, algorithmic bytes per call, label).
+    Builders allocate their inputs (drawn on the GPU) and outputs."""
     import torch
 
     import reduce_residual_rmsnorm_gb300 as pkg
     from reduce_residual_rmsnorm_gb300 import workloads as wl
 
-    rows = {}
-    with torch.cuda.stream(stream):
-        # kAllReduce on the R=8, T=4096, H=7168 inputs
-        shape = wl.WORKLOADS["C2"]
-        inp = wl.fused_inputs(shape, seed=0, device=dev)
-        out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
-        ms = time_launches(lambda: pkg.ts_fused_reduce_norm(0, inp["partials"], allreduce_out=out,
-                                                            stream=stream), iters, stream)
-        rows["kAllReduce R=8 T=4096 H=7168"] = roofline_entry(fused_bytes(0, 8, 4096, 7168), ms, peak)
-        del inp, out
+    def c2(pattern, pdl=False):
+        def build(dev, stream):
+            shape = wl.WORKLOADS["C2"]
+            inp = wl.fused_inputs(shape, seed=0, device=dev)
+            T, H = shape.T, shape.H
+            outs = pkg.new_outputs(pattern, T, H, dev)
+            res = None if pattern == 0 else inp["residual"]
+            gam = None if pattern == 0 else inp["gamma"]
+            call = lambda: pkg.ts_fused_reduce_norm(pattern, inp["partials"], res, gam, EPS,  # noqa: E731
+                                                    launch_with_pdl=pdl, stream=stream, **outs)
+            return call, fused_bytes(pattern, 8, T, H)
+        return build
 
-        # FP8 per-tensor / blockwise / PartialOut on R=8, T=8192, H=7168 with outliers
-        shape = wl.WORKLOADS["C3"]
-        inp = wl.fused_inputs(shape, seed=0, device=dev)
-        T, H = shape.T, shape.H
-        res_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-        norm = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-        pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS, residual_out=res_out,
-                                 norm_out=norm, stream=stream)
-        sigma = (448.0 / norm.float().abs().max()).reshape(1).to(torch.float32)
-        q8 = torch.empty((T, H), dtype=torch.uint8, device=dev)
-        sc = torch.empty((T, H // 128), dtype=torch.float32, device=dev)
-        part = torch.empty((T, 1024), dtype=torch.bfloat16, device=dev)
-        cases = {
-            "kARResidualRMSNormFP8Quant R=8 T=8192 H=7168": (
-                2, dict(quant_out=q8), sigma, fused_bytes(2, 8, T, H)),
-            "kARResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168": (
-                6, dict(quant_out=q8, scale_out=sc), None, fused_bytes(6, 8, T, H)),
-            "kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024": (
-                7, dict(quant_out=q8, scale_out=sc, partial_norm_out=part), None, fused_bytes(7, 8, T, H, 1024)),
-            "kARResidualRMSNormPartialOut R=8 T=8192 H=7168 P=1024": (
-                8, dict(partial_norm_out=part), None, fused_bytes(8, 8, T, H, 1024)),
-        }
-        for name, (p, outs, sf, nb) in cases.items():
-            ms = time_launches(lambda: pkg.ts_fused_reduce_norm(p, inp["partials"], inp["residual"], inp["gamma"],
-                                                                EPS, sf, residual_out=res_out, stream=stream,
-                                                                **outs), iters, stream)
-            rows[name] = roofline_entry(nb, ms, peak)
-        del inp, res_out, norm, q8, sc, part
+    def c3(pattern, P=0):
+        def build(dev, stream):
+            shape = wl.WORKLOADS["C3"]
+            inp = wl.fused_inputs(shape, seed=0, device=dev)
+            T, H = shape.T, shape.H
+            sf = None
+            if pattern == 2:
+                norm = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+                pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS,
+                                         residual_out=torch.empty_like(norm), norm_out=norm, stream=stream)
+                sf = (448.0 / norm.float().abs().max()).reshape(1).to(torch.float32)
+                del norm
+            outs = pkg.new_outputs(pattern, T, H, dev, partial_cols=P)
+            call = lambda: pkg.ts_fused_reduce_norm(pattern, inp["partials"], inp["residual"], inp["gamma"],  # noqa
+                                                    EPS, sf, stream=stream, **outs)
+            return call, fused_bytes(pattern, 8, T, H, P)
+        return build
 
-        # NVFP4 on R=4, T=16384, H=5120, LINEAR and SWIZZLED_128x4
-        shape = wl.WORKLOADS["C4"]
-        inp = wl.fused_inputs(shape, seed=0, device=dev)
-        T, H = shape.T, shape.H
-        res_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-        norm = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-        pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS, residual_out=res_out,
-                                 norm_out=norm, stream=stream)
-        g = (2688.0 / norm.float().abs().max()).reshape(1).to(torch.float32)
-        q4 = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
-        for layout, swz in ((pkg.SFLayout.LINEAR, False), (pkg.SFLayout.SWIZZLED_128x4, True)):
-            sf = torch.empty(pkg.sf_swizzled_shape(T, H) if swz else (T, H // 16), dtype=torch.uint8, device=dev)
-            ms = time_launches(lambda: pkg.ts_fused_reduce_norm(3, inp["partials"], inp["residual"], inp["gamma"],
-                                                                EPS, g, residual_out=res_out, quant_out=q4,
-                                                                scale_out=sf, sf_layout=layout, stream=stream),
-                               iters, stream)
-            rows[f"kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF {layout.name}"] = roofline_entry(
-                fused_bytes(3, 4, T, H, swizzled=swz), ms, peak)
-        del inp, res_out, norm, q4, sf
+    def c4(layout):
+        def build(dev, stream):
+            shape = wl.WORKLOADS["C4"]
+            inp = wl.fused_inputs(shape, seed=0, device=dev)
+            T, H = shape.T, shape.H
+            norm = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+            pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS,
+                                     residual_out=torch.empty_like(norm), norm_out=norm, stream=stream)
+            g = (2688.0 / norm.float().abs().max()).reshape(1).to(torch.float32)
+            del norm
+            outs = pkg.new_outputs(3, T, H, dev, sf_layout=layout)
+            call = lambda: pkg.ts_fused_reduce_norm(3, inp["partials"], inp["residual"], inp["gamma"], EPS,  # noqa
+                                                    g, sf_layout=layout, stream=stream, **outs)
+            return call, fused_bytes(3, 4, T, H, sf_layout=int(layout))
+        return build
 
-        # MiniMax sharded QK-norm, R=8, T=32768, q 1024 | k 128 | v 128
+    def c5(dev, stream):
         qs = wl.WORKLOADS["C5"]
         qi = wl.qk_inputs(qs, seed=0, device=dev)
         qo = torch.empty((qs.T, qs.R * qs.q_shard), dtype=torch.bfloat16, device=dev)
         ko = torch.empty((qs.T, qs.R * qs.k_shard), dtype=torch.bfloat16, device=dev)
-        ms = time_launches(lambda: pkg.ts_qk_norm_sharded(qi["shards"], qs.q_shard, qs.k_shard, qi["q_weight"],
-                                                          qi["k_weight"], EPS, qo, ko, stream=stream), iters, stream)
-        rows["MiniMax QK-RMSNorm R=8 T=32768 Q=1024 K=128"] = roofline_entry(
-            qk_bytes(qs.R, qs.T, qs.q_shard, qs.k_shard), ms, peak)
-        del qi, qo, ko
+        call = lambda: pkg.ts_qk_norm_sharded(qi["shards"], qs.q_shard, qs.k_shard, qi["q_weight"],  # noqa
+                                              qi["k_weight"], EPS, qo, ko, stream=stream)
+        return call, qk_bytes(qs.R, qs.T, qs.q_shard, qs.k_shard)
 
-        # latency case: R=2, T=16, H=4096 (L2-resident; reported in us)
+    def single(dev, stream):
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(0)
+        sh = torch.randn((8, 32768, 768), generator=gen, device=dev).to(torch.bfloat16)
+        w = (torch.rand(8 * 768, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
+        so = torch.empty((32768, 8 * 768), dtype=torch.bfloat16, device=dev)
+        call = lambda: pkg.ts_rms_norm_sharded(sh, 768, w, EPS, so, stream=stream)  # noqa: E731
+        return call, rms_sharded_bytes(8, 32768, 768)
+
+    def c1(dev, stream):
         shape = wl.WORKLOADS["C1"]
         inp = wl.fused_inputs(shape, seed=0, device=dev)
-        ro = torch.empty((16, 4096), dtype=torch.bfloat16, device=dev)
-        no = torch.empty((16, 4096), dtype=torch.bfloat16, device=dev)
+        outs = pkg.new_outputs(1, 16, 4096, dev)
         call = lambda: pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS,  # noqa
-                                                residual_out=ro, norm_out=no, stream=stream)
-        ms_stream = time_launches(call, max(iters, 200), stream)
-        graph = torch.cuda.CUDAGraph()
-        call()
-        torch.cuda.synchronize()
-        with torch.cuda.graph(graph, stream=stream):
-            for _ in range(100):
+                                                stream=stream, **outs)
+        return call, fused_bytes(1, 2, 16, 4096)
+
+    return {
+        "c2-p1": ("kARResidualRMSNorm R=8 T=4096 H=7168 launch_with_pdl", c2(1, True)),
+        "c2-p1-nopdl": ("kARResidualRMSNorm R=8 T=4096 H=7168 (plain launch)", c2(1)),
+        "c2-p0": ("kAllReduce R=8 T=4096 H=7168", c2(0)),
+        "c3-p2": ("kARResidualRMSNormFP8Quant R=8 T=8192 H=7168", c3(2)),
+        "c3-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168", c3(6)),
+        "c3-p7": ("kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024", c3(7, 1024)),
+        "c3-p8": ("kARResidualRMSNormPartialOut R=8 T=8192 H=7168 P=1024", c3(8, 1024)),
+        "c4-p3-linear": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF LINEAR", c4(2)),
+        "c4-p3-swizzled": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF SWIZZLED_128x4", c4(0)),
+        "c4-p3-swizzled8": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF SWIZZLED_8x4", c4(1)),
+        "c5-qk": ("MiniMax QK-RMSNorm R=8 T=32768 Q=1024 K=128", c5),
+        "single-768": ("single-matrix sharded RMSNorm R=8 T=32768 W=768", single),
+        "c1-p1": ("kARResidualRMSNorm R=2 T=16 H=4096 (latency)", c1),
+    }
+
+
+def measure_rows(dev, stream, peak: float, iters: int) -> dict:
+    import torch
+
+    rows = {}
+    for key, (label, build) in _case_builders().items():
+        if key == "c2-p1":
+            continue  # the headline step, timed in run_ours
+        with torch.cuda.stream(stream):
+            call, nbytes = build(dev, stream)
+            if key == "c1-p1":  # L2-resident latency case: stream launches and a CUDA graph
+                ms_stream = time_launches(call, max(iters, 200), stream)
+                graph = torch.cuda.CUDAGraph()
                 call()
-        ms_graph = time_launches(graph.replay, 20, stream) / 100
-        rows["kARResidualRMSNorm R=2 T=16 H=4096 (latency)"] = {
-            "us_stream_launch": ms_stream * 1e3, "us_in_cuda_graph": ms_graph * 1e3,
-            "bytes": fused_bytes(1, 2, 16, 4096)}
-        del inp, ro, no, graph
-    torch.cuda.synchronize()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(graph, stream=stream):
+                    for _ in range(100):
+                        call()
+                ms_graph = time_launches(graph.replay, 20, stream) / 100
+                rows[label] = {"us_stream_launch": ms_stream * 1e3, "us_in_cuda_graph": ms_graph * 1e3,
+                               "bytes": nbytes}
+                del graph
+            else:
+                rows[label] = roofline_entry(nbytes, time_launches(call, iters, stream), peak)
+        del call
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
     return rows
+
+
+def profile_case(key: str, launches: int) -> None:
+    """Set up one named workload and launch it ``launches`` times (for ncu)."""
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    label, build = _case_builders()[key]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        call, nbytes = build(dev, stream)
+        torch.cuda.synchronize()
+        for _ in range(launches):
+            call()
+    torch.cuda.synchronize()
+    print(json.dumps({"case": key, "label": label, "launches": launches, "bytes_per_launch": nbytes}))
 
 
 def run_ours(args):
@@ -429,7 +485,7 @@ def run_ours(args):
 
     def step():
         pkg.ts_fused_reduce_norm(1, parts, res, gamma, EPS, residual_out=res_out, norm_out=norm_out,
-                                 stream=stream)
+                                 launch_with_pdl=True, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -464,7 +520,7 @@ def run_ours(args):
         d_parts.copy_(h_parts, non_blocking=True)
         d_res.copy_(h_res, non_blocking=True)
         pkg.ts_fused_reduce_norm(1, d_parts, d_res, gamma, EPS, residual_out=res_out, norm_out=norm_out,
-                                 stream=stream)
+                                 launch_with_pdl=True, stream=stream)
         h_out_res.copy_(res_out, non_blocking=True)
         h_out_norm.copy_(norm_out, non_blocking=True)
 
@@ -493,7 +549,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "pattern": 1, "R": R, "T": T, "H": H,
-                       "bytes_per_step": nbytes,
+                       "launch_with_pdl": True, "bytes_per_step": nbytes,
                        "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB per step > 129 MB); no flush",
                        "parallelism": f"replicas x{world} (rows are independent; no collective)"},
             "achieved_gbs": achieved,
@@ -520,10 +576,15 @@ def main(argv=None):
     ap.add_argument("--no-rows", action="store_true", help="skip the other patterns/workloads")
     ap.add_argument("--row-iters", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile-case", default=None,
+                    help="only set up this named workload and launch it --launches times (for ncu)")
+    ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.profile_case:
+        profile_case(args.profile_case, args.launches)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -63,6 +63,17 @@ typedef enum {
     TS_ERR_LAUNCH = -7       /* the CUDA launch failed                                    */
 } ts_status_t;
 
+/* Launch flags (the `flags` argument of the compute calls). */
+enum {
+    /* Programmatic dependent launch (the pages' `launch_with_pdl`): the kernel
+     * is launched with programmatic stream serialisation, so its launch and
+     * prologue overlap the tail of the previous kernel in the stream; it waits
+     * (griddepcontrol.wait) for that kernel to complete before it touches any
+     * memory, and lets the next kernel start launching once its own loads are
+     * issued.  Results are identical with and without the flag. */
+    TS_FLAG_PDL = 1u
+};
+
 /* Codes identical to `AllReduceFusionPattern` (tokenspeed trtllm.py). */
 typedef enum {
     TS_AR = 0,                                 /* kAllReduce                                  */
@@ -79,7 +90,7 @@ typedef enum {
 /* Codes identical to `QuantizationSFLayout` (tokenspeed trtllm.py). */
 typedef enum {
     TS_SF_SWIZZLED_128x4 = 0,
-    TS_SF_SWIZZLED_8x4 = 1, /* not implemented: TS_ERR_UNSUPPORTED */
+    TS_SF_SWIZZLED_8x4 = 1,
     TS_SF_LINEAR = 2
 } ts_sf_layout_t;
 
@@ -121,6 +132,12 @@ typedef enum {
  *                       columns; SF (m, k) at byte
  *                       ((m/128)*(Kp/4) + k/4)*512 + (m%32)*16 + ((m%128)/32)*4 + k%4
  *                       with Kp = ceil(H/64)*4.  Padding bytes are written as 0.
+ *                       TS_SF_SWIZZLED_8x4: uint8 [ceil(T/8)*8, Kp] in 32-byte
+ *                       tiles of 8 rows x 4 columns, row-major inside a tile:
+ *                       SF (m, k) at byte ((m/8)*(Kp/4) + k/4)*32 + (m%8)*4 + k%4.
+ *                       Padding bytes are written as 0.  (The pages name both
+ *                       swizzled layouts without defining them; these are the
+ *                       library's definitions.)
  *   sf_layout         ts_sf_layout_t (patterns 3, 5; ignored otherwise).
  */
 typedef struct {
@@ -162,11 +179,12 @@ typedef struct {
  *   H             hidden size: multiple of 8, <= 16384; multiple of 128 for
  *                 patterns 6, 7; multiple of 16 for patterns 3, 5.
  *   outs          host pointer to the output set (see ts_outs_t).
+ *   flags         0 or TS_FLAG_PDL; other bits: TS_ERR_UNSUPPORTED.
  *   stream        cudaStream_t.
  */
 TS_API int ts_fused_reduce_norm(int pattern, const void *const *partials, int R, const void *residual,
-                         const void *gamma, float eps, const float *scale_factor, int64_t T,
-                         int64_t H, const ts_outs_t *outs, void *stream);
+                                const void *gamma, float eps, const float *scale_factor, int64_t T,
+                                int64_t H, const ts_outs_t *outs, uint32_t flags, void *stream);
 
 /*
  * ts_qk_norm_sharded: MiniMax tensor-parallel QK-RMSNorm with the R shards
@@ -194,12 +212,37 @@ TS_API int ts_fused_reduce_norm(int pattern, const void *const *partials, int R,
  *   q_out, ldq    bf16 [T, ldq], ldq >= R*Q, multiple of 8: shard r's block at
  *                 columns r*Q .. r*Q+Q (the unsharded, hidden-concatenated layout).
  *   k_out, ldk    bf16 [T, ldk], ldk >= R*K, multiple of 8.
+ *   flags         0 or TS_FLAG_PDL.
  *   Outputs must not overlap the shards, the weights or each other.
  */
 TS_API int ts_qk_norm_sharded(const void *const *qkv_shards, int R, int64_t T, int64_t row_stride,
-                       int64_t q_shard, int64_t k_shard, const void *q_weight,
-                       const void *k_weight, float eps, void *q_out, int64_t ldq, void *k_out,
-                       int64_t ldk, void *stream);
+                              int64_t q_shard, int64_t k_shard, const void *q_weight,
+                              const void *k_weight, float eps, void *q_out, int64_t ldq, void *k_out,
+                              int64_t ldk, uint32_t flags, void *stream);
+
+/*
+ * ts_rms_norm_sharded: single-matrix RMSNorm over a hidden dim split in R
+ * shards resident on this GPU (tokenspeed trtllm.py `minimax_allreduce_rms`:
+ * the all-reduce of the per-token variance, then each shard's slice of the
+ * norm with its slice of the weight), the one-segment form of the QK norm:
+ *
+ *   v_r[t] = sum_{j<W} x_r[t,j]^2 / W                                   fp32
+ *   V[t]   = sum over r ascending of v_r[t]                             fp32
+ *   out[t, r*W + j] = bf16((x_r[t,j] * rsqrt(V[t]/R + eps)) * weight[r*W + j])
+ *
+ *   shards        host array of R device pointers, shard r bf16 [T, row_stride]
+ *                 (its slice in the first W columns).
+ *   R             1..16.     T: tokens, >= 0 (T == 0 returns TS_OK).
+ *   row_stride    multiple of 8, >= W.
+ *   width (W)     8 <= W <= 4096, multiple of 8.
+ *   weight        bf16 [R*W].
+ *   out, ldo      bf16 [T, ldo], ldo >= R*W, multiple of 8; shard r's block at
+ *                 columns r*W .. r*W+W.  Must not overlap the inputs.
+ *   flags         0 or TS_FLAG_PDL.
+ */
+TS_API int ts_rms_norm_sharded(const void *const *shards, int R, int64_t T, int64_t row_stride,
+                               int64_t width, const void *weight, float eps, void *out, int64_t ldo,
+                               uint32_t flags, void *stream);
 
 /* Static text for a ts_status_t value ("TS_OK", "TS_ERR_SHAPE", ...). */
 TS_API const char *ts_status_string(int status);

@@ -63,7 +63,10 @@ class TsOuts(ctypes.Structure):
     ]
 
 
-EXPORTS = ("ts_fused_reduce_norm", "ts_qk_norm_sharded", "ts_status_string", "ts_last_error_detail")
+EXPORTS = ("ts_fused_reduce_norm", "ts_qk_norm_sharded", "ts_rms_norm_sharded", "ts_status_string",
+           "ts_last_error_detail")
+
+TS_FLAG_PDL = 1
 
 
 def library(path: str | None = None):
@@ -80,12 +83,16 @@ def library(path: str | None = None):
                                "(python -c 'import __graft_entry__ as g; g.build()')")
         lib = ctypes.CDLL(p)
         vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        u32 = ctypes.c_uint32
         lib.ts_fused_reduce_norm.argtypes = [ctypes.c_int, ctypes.POINTER(vp), ctypes.c_int, vp, vp,
-                                             ctypes.c_float, vp, i64, i64, ctypes.POINTER(TsOuts), vp]
+                                             ctypes.c_float, vp, i64, i64, ctypes.POINTER(TsOuts), u32, vp]
         lib.ts_fused_reduce_norm.restype = ctypes.c_int
         lib.ts_qk_norm_sharded.argtypes = [ctypes.POINTER(vp), ctypes.c_int, i64, i64, i64, i64, vp, vp,
-                                           ctypes.c_float, vp, i64, vp, i64, vp]
+                                           ctypes.c_float, vp, i64, vp, i64, u32, vp]
         lib.ts_qk_norm_sharded.restype = ctypes.c_int
+        lib.ts_rms_norm_sharded.argtypes = [ctypes.POINTER(vp), ctypes.c_int, i64, i64, i64, vp,
+                                            ctypes.c_float, vp, i64, u32, vp]
+        lib.ts_rms_norm_sharded.restype = ctypes.c_int
         lib.ts_status_string.argtypes = [ctypes.c_int]
         lib.ts_status_string.restype = ctypes.c_char_p
         lib.ts_last_error_detail.argtypes = []
@@ -134,9 +141,19 @@ def _rows(ts: torch.Tensor | Sequence[torch.Tensor], name: str) -> list[torch.Te
     return list(ts)
 
 
+def sf_shape(T: int, H: int, sf_layout: int = SFLayout.LINEAR) -> tuple[int, int]:
+    """Shape of the NVFP4 scale-factor buffer for [T, H] values in ``sf_layout``
+    (the swizzled layouts pad rows to 128 or 8 and columns to 4)."""
+    layout = int(sf_layout)
+    if layout == SFLayout.LINEAR:
+        return T, H // 16
+    tile = 128 if layout == SFLayout.SWIZZLED_128x4 else 8
+    return (T + tile - 1) // tile * tile, (H // 16 + 3) // 4 * 4
+
+
 def sf_swizzled_shape(T: int, H: int) -> tuple[int, int]:
     """Shape of the padded SWIZZLED_128x4 scale-factor buffer for [T, H] values."""
-    return (T + 127) // 128 * 128, (H // 16 + 3) // 4 * 4
+    return sf_shape(T, H, SFLayout.SWIZZLED_128x4)
 
 
 def new_outputs(pattern: int, T: int, H: int, device="cuda", partial_cols: int = 0,
@@ -157,8 +174,7 @@ def new_outputs(pattern: int, T: int, H: int, device="cuda", partial_cols: int =
         out["quant_out"] = e(T, H, dt=torch.uint8)
     if p in (3, 5):
         out["quant_out"] = e(T, H // 2, dt=torch.uint8)
-        shape = sf_swizzled_shape(T, H) if int(sf_layout) == SFLayout.SWIZZLED_128x4 else (T, H // 16)
-        out["scale_out"] = e(*shape, dt=torch.uint8)
+        out["scale_out"] = e(*sf_shape(T, H, sf_layout), dt=torch.uint8)
     if p in (6, 7):
         out["scale_out"] = e(T, H // 128, dt=torch.float32)
     return out
@@ -173,13 +189,15 @@ def ts_fused_reduce_norm(pattern: int, partials, residual: torch.Tensor | None =
                          partial_norm_out: torch.Tensor | None = None,
                          quant_out: torch.Tensor | None = None,
                          scale_out: torch.Tensor | None = None,
-                         sf_layout: int = SFLayout.LINEAR, stream=None) -> None:
+                         sf_layout: int = SFLayout.LINEAR, launch_with_pdl: bool = False,
+                         stream=None) -> None:
     """Run one AllReduceFusionPattern (see include/ts_fused_norm.h).
 
     ``partials``: R CUDA bf16 tensors [T, H] (or one [R, T, H] tensor).
     ``scale_factor``: device fp32 tensor of one element, or a Python float
     (then copied to the device first, as trtllm.py's wrapper does).
     ``partial_norm_out``'s width gives partial_cols.
+    ``launch_with_pdl``: programmatic dependent launch (TS_FLAG_PDL).
     """
     parts = [_dev(p, "partials[%d]" % i, torch.bfloat16) for i, p in enumerate(_rows(partials, "partials"))]
     T, H = parts[0].shape
@@ -204,12 +222,13 @@ def ts_fused_reduce_norm(pattern: int, partials, residual: torch.Tensor | None =
     arr = (ctypes.c_void_p * len(parts))(*[p.data_ptr() for p in parts])
     _check(library().ts_fused_reduce_norm(int(pattern), arr, len(parts), _ptr(residual), _ptr(gamma),
                                           float(eps), _ptr(scale_factor), int(T), int(H),
-                                          ctypes.byref(outs), _stream(stream)))
+                                          ctypes.byref(outs), TS_FLAG_PDL if launch_with_pdl else 0,
+                                          _stream(stream)))
 
 
 def ts_qk_norm_sharded(shards, q_shard: int, k_shard: int, q_weight: torch.Tensor,
                        k_weight: torch.Tensor, eps: float = 1e-6, q_out: torch.Tensor | None = None,
-                       k_out: torch.Tensor | None = None, stream=None):
+                       k_out: torch.Tensor | None = None, launch_with_pdl: bool = False, stream=None):
     """Sharded MiniMax QK-RMSNorm (see include/ts_fused_norm.h).
 
     ``shards``: R CUDA bf16 tensors [T, >= q_shard + k_shard] with unit column
@@ -239,5 +258,35 @@ def ts_qk_norm_sharded(shards, q_shard: int, k_shard: int, q_weight: torch.Tenso
     _check(library().ts_qk_norm_sharded(arr, R, int(T), int(stride), int(q_shard), int(k_shard),
                                         _ptr(q_weight), _ptr(k_weight), float(eps), _ptr(q_out),
                                         int(q_out.stride(0)), _ptr(k_out), int(k_out.stride(0)),
-                                        _stream(stream)))
+                                        TS_FLAG_PDL if launch_with_pdl else 0, _stream(stream)))
     return q_out, k_out
+
+
+def ts_rms_norm_sharded(shards, width: int, weight: torch.Tensor, eps: float = 1e-6,
+                        out: torch.Tensor | None = None, launch_with_pdl: bool = False, stream=None):
+    """Single-matrix sharded RMSNorm (see include/ts_fused_norm.h).
+
+    ``shards``: R CUDA bf16 tensors [T, >= width] with unit column stride and a
+    common row stride (or one [R, T, row] tensor); ``weight``: bf16 [R*width].
+    Returns ``out`` [T, R*width] (allocated if None).
+    """
+    sh = [_dev(s, "shards[%d]" % i, torch.bfloat16) for i, s in enumerate(_rows(shards, "shards"))]
+    T = sh[0].shape[0]
+    stride = sh[0].stride(0)
+    for s in sh:
+        if s.dim() != 2 or s.shape[0] != T or s.stride(1) != 1 or s.stride(0) != stride:
+            raise ValueError("shards must share T and the row stride, with unit column stride")
+        if s.shape[1] < width:
+            raise ValueError("a shard row is narrower than width")
+    R = len(sh)
+    _dev(weight, "weight", torch.bfloat16)
+    if out is None:
+        out = torch.empty((T, R * width), dtype=torch.bfloat16, device=sh[0].device)
+    _dev(out, "out", torch.bfloat16)
+    if out.dim() != 2 or out.stride(1) != 1:
+        raise ValueError("out must be 2-D with unit column stride")
+    arr = (ctypes.c_void_p * R)(*[s.data_ptr() for s in sh])
+    _check(library().ts_rms_norm_sharded(arr, R, int(T), int(stride), int(width), _ptr(weight), float(eps),
+                                         _ptr(out), int(out.stride(0)), TS_FLAG_PDL if launch_with_pdl else 0,
+                                         _stream(stream)))
+    return out

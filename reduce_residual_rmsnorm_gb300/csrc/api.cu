@@ -72,6 +72,7 @@ const char *const kOutputNames[6] = {"allreduce_out", "residual_out", "norm_out"
                                      "partial_norm_out", "quant_out", "scale_out"};
 
 constexpr int64_t kMaxH = 16384;
+constexpr uint32_t kKnownFlags = TS_FLAG_PDL;
 constexpr int64_t kMaxRows = 0x7FFFFFFFLL;
 
 }  // namespace
@@ -96,7 +97,7 @@ extern "C" const char *ts_last_error_detail(void) { return g_detail; }
 extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, int R,
                                     const void *residual, const void *gamma, float eps,
                                     const float *scale_factor, int64_t T, int64_t H,
-                                    const ts_outs_t *outs, void *stream)
+                                    const ts_outs_t *outs, uint32_t flags, void *stream)
 {
     if (pattern < 0 || pattern > 8)
         return fail(TS_ERR_BAD_PATTERN, "pattern %d is not an AllReduceFusionPattern code (0..8)", pattern);
@@ -119,6 +120,8 @@ extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, in
         return fail(TS_ERR_SHAPE, "NVFP4 needs H %% 16 == 0 (H = %lld)", (long long)H);
     if (outs->reserved != 0)
         return fail(TS_ERR_UNSUPPORTED, "ts_outs_t.reserved must be 0");
+    if (flags & ~kKnownFlags)
+        return fail(TS_ERR_UNSUPPORTED, "unknown flag bits 0x%x", flags & ~kKnownFlags);
 
     // inputs (with T == 0 the per-row buffers may be NULL: empty tensors)
     const bool empty = T == 0;
@@ -170,22 +173,20 @@ extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, in
             return fail(TS_ERR_SHAPE, "partial_cols = %lld must be in 1..H and a multiple of 8",
                         (long long)P);
     }
-    bool swz = false;
+    int layout = TS_SF_LINEAR;
     if (fp4) {
-        if (outs->sf_layout == TS_SF_SWIZZLED_128x4)
-            swz = true;
-        else if (outs->sf_layout == TS_SF_SWIZZLED_8x4)
-            return fail(TS_ERR_UNSUPPORTED, "SF layout SWIZZLED_8x4 is not implemented");
-        else if (outs->sf_layout != TS_SF_LINEAR)
-            return fail(TS_ERR_BAD_PATTERN, "sf_layout %d is not a QuantizationSFLayout code",
-                        (int)outs->sf_layout);
+        layout = outs->sf_layout;
+        if (layout != TS_SF_SWIZZLED_128x4 && layout != TS_SF_SWIZZLED_8x4 && layout != TS_SF_LINEAR)
+            return fail(TS_ERR_BAD_PATTERN, "sf_layout %d is not a QuantizationSFLayout code", layout);
     }
+    const bool swz = layout != TS_SF_LINEAR;
 
     // aliasing: outputs disjoint from each other and from the inputs, except
     // allreduce_out == partials[0] and residual_out == residual (in place)
     const int64_t elems = T * H;
     const int64_t n_sf = H / 16;
-    const int64_t sf_rows = swz ? (T + 127) / 128 * 128 : T;
+    const int64_t row_tile = layout == TS_SF_SWIZZLED_128x4 ? 128 : (layout == TS_SF_SWIZZLED_8x4 ? 8 : 1);
+    const int64_t sf_rows = (T + row_tile - 1) / row_tile * row_tile;
     const int64_t sf_cols = swz ? (n_sf + 3) / 4 * 4 : n_sf;
     int64_t quant_bytes = fp4 ? elems / 2 : elems;
     int64_t scale_bytes = fp4 ? sf_rows * sf_cols : (fp8_block ? T * (H / 128) * 4 : 0);
@@ -236,7 +237,7 @@ extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, in
     a.partial_cols = P;
     a.quant_out = static_cast<uint8_t *>(outs->quant_out);
     a.scale_out = outs->scale_out;
-    a.sf_swizzled = swz ? 1 : 0;
+    a.sf_layout = layout;
     a.sf_rows = sf_rows;
     a.sf_cols = sf_cols;
 
@@ -251,65 +252,75 @@ extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, in
     case 5: ep = Epilogue::kFp4; break;
     default: ep = Epilogue::kFp8Block; break;
     }
-    const cudaError_t err = tsfn::launch_fused(ep, a, static_cast<cudaStream_t>(stream));
+    const cudaError_t err =
+        tsfn::launch_fused(ep, a, (flags & TS_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess)
         return fail(TS_ERR_LAUNCH, "kernel launch failed: %s (%s)", cudaGetErrorName(err),
                     cudaGetErrorString(err));
     return ok();
 }
 
-extern "C" int ts_qk_norm_sharded(const void *const *qkv_shards, int R, int64_t T,
-                                  int64_t row_stride, int64_t q_shard, int64_t k_shard,
-                                  const void *q_weight, const void *k_weight, float eps,
-                                  void *q_out, int64_t ldq, void *k_out, int64_t ldk, void *stream)
+namespace {
+
+// Checks and launch shared by ts_qk_norm_sharded and ts_rms_norm_sharded
+// (K == 0, no k segment).
+int sharded_norm(const char *what, const void *const *shards, int R, int64_t T, int64_t row_stride,
+                 int64_t Q, int64_t K, const void *q_weight, const void *k_weight, float eps,
+                 void *q_out, int64_t ldq, void *k_out, int64_t ldk, uint32_t flags, void *stream)
 {
-    if (qkv_shards == nullptr)
-        return fail(TS_ERR_NULL, "qkv_shards is NULL");
+    const bool has_k = K != 0;
+    if (shards == nullptr)
+        return fail(TS_ERR_NULL, "%s is NULL", what);
     if (R < 1 || R > tsfn::kMaxR)
         return fail(TS_ERR_SHAPE, "R = %d outside 1..%d", R, tsfn::kMaxR);
     if (T < 0 || T > kMaxRows)
         return fail(TS_ERR_SHAPE, "T = %lld outside 0..%lld", (long long)T, (long long)kMaxRows);
-    if (q_shard < 8 || q_shard % 8 != 0 || k_shard < 8 || k_shard % 8 != 0)
-        return fail(TS_ERR_SHAPE, "q_shard = %lld and k_shard = %lld must be positive multiples of 8",
-                    (long long)q_shard, (long long)k_shard);
-    if (q_shard > 4096 || k_shard > 1024)
-        return fail(TS_ERR_UNSUPPORTED, "q_shard <= 4096 and k_shard <= 1024 are supported");
-    if (row_stride % 8 != 0 || row_stride < q_shard + k_shard)
-        return fail(TS_ERR_SHAPE, "row_stride = %lld must be a multiple of 8 and >= q_shard + k_shard",
+    if (flags & ~kKnownFlags)
+        return fail(TS_ERR_UNSUPPORTED, "unknown flag bits 0x%x", flags & ~kKnownFlags);
+    if (Q < 8 || Q % 8 != 0 || (has_k && (K < 8 || K % 8 != 0)))
+        return fail(TS_ERR_SHAPE, "segment widths (%lld, %lld) must be positive multiples of 8",
+                    (long long)Q, (long long)K);
+    if (Q > 4096 || K > 1024)
+        return fail(TS_ERR_UNSUPPORTED, "segment widths up to 4096 (q / single) and 1024 (k) are supported");
+    if (row_stride % 8 != 0 || row_stride < Q + K)
+        return fail(TS_ERR_SHAPE, "row_stride = %lld must be a multiple of 8 and cover the segments",
                     (long long)row_stride);
-    if (ldq % 8 != 0 || ldq < R * q_shard)
-        return fail(TS_ERR_SHAPE, "ldq = %lld must be a multiple of 8 and >= R*q_shard", (long long)ldq);
-    if (ldk % 8 != 0 || ldk < R * k_shard)
+    if (ldq % 8 != 0 || ldq < R * Q)
+        return fail(TS_ERR_SHAPE, "output leading dimension %lld must be a multiple of 8 and >= R*width",
+                    (long long)ldq);
+    if (has_k && (ldk % 8 != 0 || ldk < R * K))
         return fail(TS_ERR_SHAPE, "ldk = %lld must be a multiple of 8 and >= R*k_shard", (long long)ldk);
     const bool empty = T == 0;  // per-token buffers may then be NULL (empty tensors)
     for (int r = 0; r < R; ++r) {
-        if (qkv_shards[r] == nullptr && !empty)
-            return fail(TS_ERR_NULL, "qkv_shards[%d] is NULL", r);
-        if (!aligned(qkv_shards[r], 16))
-            return fail(TS_ERR_ALIGN, "qkv_shards[%d] is not 16-byte aligned", r);
+        if (shards[r] == nullptr && !empty)
+            return fail(TS_ERR_NULL, "%s[%d] is NULL", what, r);
+        if (!aligned(shards[r], 16))
+            return fail(TS_ERR_ALIGN, "%s[%d] is not 16-byte aligned", what, r);
     }
     const void *const ptrs[4] = {q_weight, k_weight, q_out, k_out};
-    const char *const names[4] = {"q_weight", "k_weight", "q_out", "k_out"};
+    const char *const names[4] = {has_k ? "q_weight" : "weight", "k_weight", has_k ? "q_out" : "out", "k_out"};
     for (int i = 0; i < 4; ++i) {
+        if (!has_k && (i == 1 || i == 3))
+            continue;
         if (ptrs[i] == nullptr && !(empty && i >= 2))
             return fail(TS_ERR_NULL, "%s is NULL", names[i]);
         if (!aligned(ptrs[i], 16))
             return fail(TS_ERR_ALIGN, "%s is not 16-byte aligned", names[i]);
     }
     if (T > 0) {
-        const Span qo = span(q_out, ((T - 1) * ldq + R * q_shard) * 2, "q_out");
-        const Span ko = span(k_out, ((T - 1) * ldk + R * k_shard) * 2, "k_out");
+        const Span qo = span(q_out, ((T - 1) * ldq + R * Q) * 2, names[2]);
+        const Span ko = span(has_k ? k_out : nullptr, has_k ? ((T - 1) * ldk + R * K) * 2 : 0, "k_out");
         if (overlap(qo, ko))
             return fail(TS_ERR_ALIAS, "q_out overlaps k_out");
-        const Span ins[2] = {span(q_weight, R * q_shard * 2, "q_weight"),
-                             span(k_weight, R * k_shard * 2, "k_weight")};
+        const Span ins[2] = {span(q_weight, R * Q * 2, names[0]),
+                             span(has_k ? k_weight : nullptr, R * K * 2, "k_weight")};
         for (const Span &o : {qo, ko}) {
             for (const Span &in : ins)
                 if (overlap(o, in))
                     return fail(TS_ERR_ALIAS, "%s overlaps %s", o.name, in.name);
             for (int r = 0; r < R; ++r)
-                if (overlap(o, span(qkv_shards[r], ((T - 1) * row_stride + q_shard + k_shard) * 2, "")))
-                    return fail(TS_ERR_ALIAS, "%s overlaps qkv_shards[%d]", o.name, r);
+                if (overlap(o, span(shards[r], ((T - 1) * row_stride + Q + K) * 2, "")))
+                    return fail(TS_ERR_ALIAS, "%s overlaps %s[%d]", o.name, what, r);
         }
     }
     if (T == 0)
@@ -317,22 +328,45 @@ extern "C" int ts_qk_norm_sharded(const void *const *qkv_shards, int R, int64_t 
 
     tsfn::QKArgs a{};
     for (int r = 0; r < R; ++r)
-        a.shards[r] = static_cast<const uint16_t *>(qkv_shards[r]);
+        a.shards[r] = static_cast<const uint16_t *>(shards[r]);
     a.R = R;
     a.T = T;
     a.row_stride = row_stride;
-    a.Q = (int)q_shard;
-    a.K = (int)k_shard;
+    a.Q = (int)Q;
+    a.K = (int)K;
     a.q_weight = static_cast<const uint16_t *>(q_weight);
-    a.k_weight = static_cast<const uint16_t *>(k_weight);
+    a.k_weight = has_k ? static_cast<const uint16_t *>(k_weight) : nullptr;
     a.eps = eps;
     a.q_out = static_cast<uint16_t *>(q_out);
     a.ldq = ldq;
-    a.k_out = static_cast<uint16_t *>(k_out);
-    a.ldk = ldk;
-    const cudaError_t err = tsfn::launch_qk(a, static_cast<cudaStream_t>(stream));
+    a.k_out = has_k ? static_cast<uint16_t *>(k_out) : nullptr;
+    a.ldk = has_k ? ldk : 0;
+    const cudaError_t err =
+        tsfn::launch_qk(a, (flags & TS_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess)
         return fail(TS_ERR_LAUNCH, "kernel launch failed: %s (%s)", cudaGetErrorName(err),
                     cudaGetErrorString(err));
     return ok();
+}
+
+}  // namespace
+
+extern "C" int ts_qk_norm_sharded(const void *const *qkv_shards, int R, int64_t T,
+                                  int64_t row_stride, int64_t q_shard, int64_t k_shard,
+                                  const void *q_weight, const void *k_weight, float eps,
+                                  void *q_out, int64_t ldq, void *k_out, int64_t ldk, uint32_t flags,
+                                  void *stream)
+{
+    if (k_shard == 0)
+        return fail(TS_ERR_SHAPE, "k_shard must be a positive multiple of 8 (use ts_rms_norm_sharded for one segment)");
+    return sharded_norm("qkv_shards", qkv_shards, R, T, row_stride, q_shard, k_shard, q_weight, k_weight,
+                        eps, q_out, ldq, k_out, ldk, flags, stream);
+}
+
+extern "C" int ts_rms_norm_sharded(const void *const *shards, int R, int64_t T, int64_t row_stride,
+                                   int64_t width, const void *weight, float eps, void *out, int64_t ldo,
+                                   uint32_t flags, void *stream)
+{
+    return sharded_norm("shards", shards, R, T, row_stride, width, 0, weight, nullptr, eps, out, ldo,
+                        nullptr, 0, flags, stream);
 }

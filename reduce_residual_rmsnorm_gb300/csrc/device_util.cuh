@@ -143,6 +143,22 @@ __device__ __forceinline__ float e4m3_value(uint32_t c)
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+
+// Wait until the grid this launch depends on (the previous kernel in the
+// stream, when launched with programmatic stream serialisation) has completed
+// and its memory is visible.  A no-op for a normal launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel in the stream start launching (it still waits in
+// pdl_wait() for this grid to complete).  A no-op for a normal launch.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // reductions
 // ---------------------------------------------------------------------------
 

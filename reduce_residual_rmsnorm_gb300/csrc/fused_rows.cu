@@ -19,23 +19,13 @@
 // only shared memory is the per-warp partial sums of x^2.
 #include "device_util.cuh"
 #include "launch.h"
+#include "sf_layout.cuh"
 
 namespace tsfn {
 
 namespace {
 
 constexpr int kMaxThreads = 512;
-
-__device__ __forceinline__ int64_t sf_offset(const FusedArgs &a, int64_t m, int64_t k)
-{
-    if (!a.sf_swizzled)
-        return m * (a.H >> 4) + k;
-    // 512-byte tiles of 128 rows x 4 columns; inside a tile row m%128 = 32*i + j
-    // sits at 16*j + 4*i.
-    const int64_t tiles_per_band = a.sf_cols >> 2;
-    return ((m >> 7) * tiles_per_band + (k >> 2)) * 512 + (m & 31) * 16 + ((m & 127) >> 5) * 4 +
-           (k & 3);
-}
 
 template <int RB, int V, Epilogue EP>
 __global__ void __launch_bounds__(kMaxThreads) fused_rows_kernel(const __grid_constant__ FusedArgs a)
@@ -46,8 +36,9 @@ __global__ void __launch_bounds__(kMaxThreads) fused_rows_kernel(const __grid_co
     const int64_t row = blockIdx.x;
     const int nc = (int)(a.H >> 3);
 
+    pdl_wait();
     if constexpr (EP == Epilogue::kFp4) {
-        if (row >= a.T) {  // a padding row of the swizzled SF buffer: zeros only
+        if (row >= a.T) {  // a padding row of a swizzled SF buffer: zeros only
             uint8_t *sf = static_cast<uint8_t *>(a.scale_out);
             for (int64_t k4 = tid; k4 < (a.sf_cols >> 2); k4 += nthr)
                 st_u32(sf + sf_offset(a, row, k4 * 4), 0u);
@@ -105,6 +96,7 @@ __global__ void __launch_bounds__(kMaxThreads) fused_rows_kernel(const __grid_co
                 x[v][e] = 0.0f;
         }
     }
+    pdl_launch_dependents();
     if constexpr (EP == Epilogue::kAllReduce)
         return;
 
@@ -220,7 +212,7 @@ __global__ void __launch_bounds__(kMaxThreads) fused_rows_kernel(const __grid_co
 
     if constexpr (EP == Epilogue::kFp4) {
         // zero the padding columns of this row in the swizzled layout
-        if (a.sf_swizzled && tid == 0) {
+        if (a.sf_layout != kSfLinear && tid == 0) {
             uint8_t *sfp = static_cast<uint8_t *>(a.scale_out);
             for (int64_t k = a.H >> 4; k < a.sf_cols; ++k)
                 st_u8(sfp + sf_offset(a, row, k), 0u);
@@ -229,39 +221,39 @@ __global__ void __launch_bounds__(kMaxThreads) fused_rows_kernel(const __grid_co
 }
 
 template <int RB, int V>
-cudaError_t launch_rb_v(Epilogue ep, const FusedArgs &a, int nthr, int64_t grid, cudaStream_t s)
+cudaError_t launch_rb_v(Epilogue ep, const FusedArgs &a, int nthr, int64_t grid, bool pdl, cudaStream_t s)
 {
     const dim3 g((unsigned)grid), b((unsigned)nthr);
     switch (ep) {
-    case Epilogue::kAllReduce: fused_rows_kernel<RB, V, Epilogue::kAllReduce><<<g, b, 0, s>>>(a); break;
-    case Epilogue::kNorm: fused_rows_kernel<RB, V, Epilogue::kNorm><<<g, b, 0, s>>>(a); break;
-    case Epilogue::kFp8Tensor: fused_rows_kernel<RB, V, Epilogue::kFp8Tensor><<<g, b, 0, s>>>(a); break;
-    case Epilogue::kFp4: fused_rows_kernel<RB, V, Epilogue::kFp4><<<g, b, 0, s>>>(a); break;
-    case Epilogue::kFp8Block: fused_rows_kernel<RB, V, Epilogue::kFp8Block><<<g, b, 0, s>>>(a); break;
+    case Epilogue::kAllReduce: return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kAllReduce>, g, b, 0, s, pdl, a);
+    case Epilogue::kNorm: return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm>, g, b, 0, s, pdl, a);
+    case Epilogue::kFp8Tensor: return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Tensor>, g, b, 0, s, pdl, a);
+    case Epilogue::kFp4: return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp4>, g, b, 0, s, pdl, a);
+    case Epilogue::kFp8Block: return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block>, g, b, 0, s, pdl, a);
     }
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 template <int RB>
-cudaError_t launch_rb(Epilogue ep, const FusedArgs &a, cudaStream_t s)
+cudaError_t launch_rb(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t s)
 {
     const int nc = (int)(a.H >> 3);
     const int V = nc <= kMaxThreads ? 1 : (nc <= 2 * kMaxThreads ? 2 : 4);
     const int per = (nc + V - 1) / V;
     const int nthr = (per + 31) / 32 * 32;
-    const int64_t grid = (ep == Epilogue::kFp4 && a.sf_swizzled) ? a.sf_rows : a.T;
-    if (V == 1) return launch_rb_v<RB, 1>(ep, a, nthr, grid, s);
-    if (V == 2) return launch_rb_v<RB, 2>(ep, a, nthr, grid, s);
-    return launch_rb_v<RB, 4>(ep, a, nthr, grid, s);
+    const int64_t grid = (ep == Epilogue::kFp4 && a.sf_layout != kSfLinear) ? a.sf_rows : a.T;
+    if (V == 1) return launch_rb_v<RB, 1>(ep, a, nthr, grid, pdl, s);
+    if (V == 2) return launch_rb_v<RB, 2>(ep, a, nthr, grid, pdl, s);
+    return launch_rb_v<RB, 4>(ep, a, nthr, grid, pdl, s);
 }
 
 }  // namespace
 
-cudaError_t launch_fused(Epilogue ep, const FusedArgs &a, cudaStream_t stream)
+cudaError_t launch_fused(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t stream)
 {
-    if (a.R <= 4) return launch_rb<4>(ep, a, stream);
-    if (a.R <= 8) return launch_rb<8>(ep, a, stream);
-    return launch_rb<16>(ep, a, stream);
+    if (a.R <= 4) return launch_rb<4>(ep, a, pdl, stream);
+    if (a.R <= 8) return launch_rb<8>(ep, a, pdl, stream);
+    return launch_rb<16>(ep, a, pdl, stream);
 }
 
 }  // namespace tsfn

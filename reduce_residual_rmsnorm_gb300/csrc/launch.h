@@ -3,12 +3,18 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 
 #include <cuda_runtime.h>
 
 namespace tsfn {
 
 constexpr int kMaxR = 16;
+
+// `QuantizationSFLayout` codes.
+constexpr int kSfSwizzled128x4 = 0;
+constexpr int kSfSwizzled8x4 = 1;
+constexpr int kSfLinear = 2;
 
 // Kinds of output epilogue; the pattern codes map onto them.
 enum class Epilogue : int {
@@ -35,8 +41,8 @@ struct FusedArgs {
     int64_t partial_cols;
     uint8_t *quant_out;
     void *scale_out;    // fp32 block scales or uint8 SFs
-    int sf_swizzled;    // 1: SWIZZLED_128x4, 0: LINEAR
-    int64_t sf_rows;    // rows of the SF buffer (T, or T padded to 128)
+    int sf_layout;      // kSfSwizzled128x4, kSfSwizzled8x4 or kSfLinear
+    int64_t sf_rows;    // rows of the SF buffer (T, or T padded to 128 / 8)
     int64_t sf_cols;    // H/16, padded to a multiple of 4 when swizzled
 };
 
@@ -56,7 +62,28 @@ struct QKArgs {
     int64_t ldk;
 };
 
-cudaError_t launch_fused(Epilogue ep, const FusedArgs &a, cudaStream_t stream);
-cudaError_t launch_qk(const QKArgs &a, cudaStream_t stream);
+// Launch `kernel` on `stream`, with programmatic stream serialisation when
+// `pdl` is set (the kernel then overlaps its launch with the previous
+// kernel's tail and waits for it in pdl_wait()).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool pdl, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+cudaError_t launch_fused(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t stream);
+// Sharded RMSNorm over one (K == 0) or two (q and k) segments of each shard row.
+cudaError_t launch_qk(const QKArgs &a, bool pdl, cudaStream_t stream);
 
 }  // namespace tsfn

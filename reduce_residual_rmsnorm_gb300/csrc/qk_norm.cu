@@ -1,6 +1,8 @@
 // MiniMax tensor-parallel QK-RMSNorm with the R shards resident on one GPU,
 // as one fused kernel (vLLM rms_norm_tp: `_minimax_qk_var_kernel`, the
-// all-reduce of the [T, 2] fp32 variance, `_minimax_rms_apply_kernel`).
+// all-reduce of the [T, 2] fp32 variance, `_minimax_rms_apply_kernel`).  With
+// no k segment (K == 0, KC == 0) the same kernel is the single-matrix sharded
+// RMSNorm of tokenspeed trtllm.py `minimax_allreduce_rms`.
 //
 // One warp per (token, shard): the warp reads the shard's q (Q values) and k
 // (K values) of the token once into registers (128-bit loads, lane l owns
@@ -31,8 +33,10 @@ __global__ void __launch_bounds__(kMaxThreads) qk_norm_kernel(const __grid_const
 
     __shared__ float mq[kMaxThreads / 32], mk[kMaxThreads / 32];
 
+    pdl_wait();
+
     const uint16_t *base = a.shards[r] + t * a.row_stride;
-    uint4 qv[QC], kv[KC];
+    uint4 qv[QC], kv[KC > 0 ? KC : 1];
 #pragma unroll
     for (int i = 0; i < QC; ++i) {
         const int c = lane + 32 * i;
@@ -68,11 +72,14 @@ __global__ void __launch_bounds__(kMaxThreads) qk_norm_kernel(const __grid_const
                 sk = fmaf(f[e], f[e], sk);
         }
     }
+    pdl_launch_dependents();
     sq = warp_sum(sq);
-    sk = warp_sum(sk);
+    if (KC > 0)
+        sk = warp_sum(sk);
     if (lane == 0) {
         mq[warp] = __fdiv_rn(sq, (float)a.Q);
-        mk[warp] = __fdiv_rn(sk, (float)a.K);
+        if (KC > 0)
+            mk[warp] = __fdiv_rn(sk, (float)a.K);
     }
     __syncthreads();
     if (!live)
@@ -81,15 +88,14 @@ __global__ void __launch_bounds__(kMaxThreads) qk_norm_kernel(const __grid_const
     float Vq = 0.0f, Vk = 0.0f;
     for (int s = 0; s < a.R; ++s) {
         Vq = __fadd_rn(Vq, mq[tl * a.R + s]);
-        Vk = __fadd_rn(Vk, mk[tl * a.R + s]);
+        if (KC > 0)
+            Vk = __fadd_rn(Vk, mk[tl * a.R + s]);
     }
     const float iq = rsqrtf(__fadd_rn(__fdiv_rn(Vq, (float)a.R), a.eps));
-    const float ik = rsqrtf(__fadd_rn(__fdiv_rn(Vk, (float)a.R), a.eps));
+    const float ik = KC > 0 ? rsqrtf(__fadd_rn(__fdiv_rn(Vk, (float)a.R), a.eps)) : 0.0f;
 
     const uint16_t *wq = a.q_weight + (int64_t)r * a.Q;
-    const uint16_t *wk = a.k_weight + (int64_t)r * a.K;
     uint16_t *qo = a.q_out + t * a.ldq + (int64_t)r * a.Q;
-    uint16_t *ko = a.k_out + t * a.ldk + (int64_t)r * a.K;
 #pragma unroll
     for (int i = 0; i < QC; ++i) {
         const int c = lane + 32 * i;
@@ -103,6 +109,10 @@ __global__ void __launch_bounds__(kMaxThreads) qk_norm_kernel(const __grid_const
             st_v4(qo + (int64_t)c * 8, pack8(y));
         }
     }
+    if constexpr (KC == 0)
+        return;
+    const uint16_t *wk = a.k_weight + (int64_t)r * a.K;
+    uint16_t *ko = a.k_out + t * a.ldk + (int64_t)r * a.K;
 #pragma unroll
     for (int i = 0; i < KC; ++i) {
         const int c = lane + 32 * i;
@@ -119,38 +129,44 @@ __global__ void __launch_bounds__(kMaxThreads) qk_norm_kernel(const __grid_const
 }
 
 template <int QC>
-cudaError_t launch_qc(const QKArgs &a, int kc, int tpc, int64_t grid, int nthr, cudaStream_t s)
+cudaError_t launch_qc(const QKArgs &a, int kc, int tpc, int64_t grid, int nthr, bool pdl, cudaStream_t s)
 {
     const dim3 g((unsigned)grid), b((unsigned)nthr);
-    if (kc == 1) qk_norm_kernel<QC, 1><<<g, b, 0, s>>>(a, tpc);
-    else if (kc == 2) qk_norm_kernel<QC, 2><<<g, b, 0, s>>>(a, tpc);
-    else qk_norm_kernel<QC, 4><<<g, b, 0, s>>>(a, tpc);
-    return cudaGetLastError();
+    switch (kc) {
+    case 0: return launch_kernel(qk_norm_kernel<QC, 0>, g, b, 0, s, pdl, a, tpc);
+    case 1: return launch_kernel(qk_norm_kernel<QC, 1>, g, b, 0, s, pdl, a, tpc);
+    case 2: return launch_kernel(qk_norm_kernel<QC, 2>, g, b, 0, s, pdl, a, tpc);
+    default: return launch_kernel(qk_norm_kernel<QC, 4>, g, b, 0, s, pdl, a, tpc);
+    }
 }
 
-int chunks_bucket(int chunks_per_lane)
+// Smallest power of two >= the number of 8-element chunks each lane owns.
+int chunks_bucket(int elems)
 {
+    if (elems == 0)
+        return 0;
+    const int per_lane = (elems / 8 + 31) / 32;
     int b = 1;
-    while (b < chunks_per_lane)
+    while (b < per_lane)
         b <<= 1;
     return b;
 }
 
 }  // namespace
 
-cudaError_t launch_qk(const QKArgs &a, cudaStream_t stream)
+cudaError_t launch_qk(const QKArgs &a, bool pdl, cudaStream_t stream)
 {
-    const int qc = chunks_bucket((a.Q / 8 + 31) / 32);  // 1..16
-    const int kc = chunks_bucket((a.K / 8 + 31) / 32);  // 1..4
-    const int tpc = a.R >= 8 ? 1 : 8 / a.R;             // tokens per CTA
+    const int qc = chunks_bucket(a.Q);      // 1..16
+    const int kc = chunks_bucket(a.K);      // 0..4
+    const int tpc = a.R >= 8 ? 1 : 8 / a.R;  // tokens per CTA
     const int nthr = tpc * a.R * 32;
     const int64_t grid = (a.T + tpc - 1) / tpc;
     switch (qc) {
-    case 1: return launch_qc<1>(a, kc, tpc, grid, nthr, stream);
-    case 2: return launch_qc<2>(a, kc, tpc, grid, nthr, stream);
-    case 4: return launch_qc<4>(a, kc, tpc, grid, nthr, stream);
-    case 8: return launch_qc<8>(a, kc, tpc, grid, nthr, stream);
-    default: return launch_qc<16>(a, kc, tpc, grid, nthr, stream);
+    case 1: return launch_qc<1>(a, kc, tpc, grid, nthr, pdl, stream);
+    case 2: return launch_qc<2>(a, kc, tpc, grid, nthr, pdl, stream);
+    case 4: return launch_qc<4>(a, kc, tpc, grid, nthr, pdl, stream);
+    case 8: return launch_qc<8>(a, kc, tpc, grid, nthr, pdl, stream);
+    default: return launch_qc<16>(a, kc, tpc, grid, nthr, pdl, stream);
     }
 }
 

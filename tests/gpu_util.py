@@ -24,7 +24,9 @@ class Guarded:
         return bool((b[:GUARD] == FILL).all() and (b[GUARD + self.nbytes:] == FILL).all())
 
 
-def guarded_outputs(pattern, T, H, device, partial_cols=0, swizzled=False, allreduce=True):
+def guarded_outputs(pattern, T, H, device, partial_cols=0, layout=2, allreduce=True):
+    """Guarded outputs of a pattern; ``layout`` is the NVFP4 SF layout code
+    (0 SWIZZLED_128x4, 1 SWIZZLED_8x4, 2 LINEAR)."""
     p = int(pattern)
     bf = torch.bfloat16
     spec = {}
@@ -40,10 +42,11 @@ def guarded_outputs(pattern, T, H, device, partial_cols=0, swizzled=False, allre
         spec["quant_out"] = ((T, H), torch.uint8)
     if p in (3, 5):
         spec["quant_out"] = ((T, H // 2), torch.uint8)
-        if swizzled:
-            spec["scale_out"] = (((T + 127) // 128 * 128, (H // 16 + 3) // 4 * 4), torch.uint8)
-        else:
+        if layout == 2:
             spec["scale_out"] = ((T, H // 16), torch.uint8)
+        else:
+            tile = 128 if layout == 0 else 8
+            spec["scale_out"] = (((T + tile - 1) // tile * tile, (H // 16 + 3) // 4 * 4), torch.uint8)
     if p in (6, 7):
         spec["scale_out"] = ((T, H // 128), torch.float32)
     return {k: Guarded(s, d, device) for k, (s, d) in spec.items()}

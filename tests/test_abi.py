@@ -70,11 +70,11 @@ class Fake:
         return p
 
 
-def _fused_call(lib, pattern=1, R=2, T=16, H=256, P=0, sf_layout=2, mutate=None):
+def _fused_call(lib, pattern=1, R=2, T=16, H=256, P=0, sf_layout=2, flags=0, mutate=None):
     f = Fake()
     parts = [f() for _ in range(R)]
     args = dict(pattern=pattern, partials=parts, R=R, residual=f(), gamma=f(), eps=1e-6,
-                scale_factor=f(), T=T, H=H)
+                scale_factor=f(), T=T, H=H, flags=flags)
     table = {0: "R-----", 1: "oRR---", 2: "oR--R-", 3: "oR--RR", 4: "oRR-R-", 5: "oRR-RR",
              6: "oR--RR", 7: "oR-RRR", 8: "oRoR--"}
     row = table.get(pattern, "oRR---")
@@ -91,7 +91,7 @@ def _fused_call(lib, pattern=1, R=2, T=16, H=256, P=0, sf_layout=2, mutate=None)
     arr = None if parts is None else (ctypes.c_void_p * len(parts))(*parts)
     st = lib.ts_fused_reduce_norm(args["pattern"], arr, args["R"], args["residual"], args["gamma"],
                                   args["eps"], args["scale_factor"], args["T"], args["H"],
-                                  ctypes.byref(o), None)
+                                  ctypes.byref(o), args["flags"], None)
     return st, lib.ts_last_error_detail().decode()
 
 
@@ -142,9 +142,9 @@ NEG_FUSED = [
     ("partial_cols 0", dict(pattern=8, P=0), SHAPE),
     ("partial_cols > H", dict(pattern=8, P=264), SHAPE),
     ("partial_cols % 8", dict(pattern=7, P=100), SHAPE),
-    ("sf layout 8x4", dict(pattern=3, sf_layout=1), UNSUPPORTED),
     ("sf layout 7", dict(pattern=5, sf_layout=7), BAD_PATTERN),
     ("reserved", dict(mutate=_set("reserved", 1)), UNSUPPORTED),
+    ("unknown flag", dict(flags=2), UNSUPPORTED),
     ("outputs overlap", dict(mutate=lambda a, o: o.update(norm_out=o["residual_out"] + 16)), ALIAS),
     ("output overlaps partial", dict(mutate=lambda a, o: o.update(norm_out=a["partials"][1])), ALIAS),
     ("allreduce_out inside partial 0", dict(pattern=0, mutate=lambda a, o: o.update(
@@ -192,15 +192,28 @@ def test_in_place_aliases_are_accepted(lib):
 # ts_qk_norm_sharded
 # ---------------------------------------------------------------------------
 
-def _qk_call(lib, R=8, T=4, stride=1280, Q=1024, K=128, ldq=None, ldk=None, mutate=None):
+def _qk_call(lib, R=8, T=4, stride=1280, Q=1024, K=128, ldq=None, ldk=None, flags=0, mutate=None):
     f = Fake()
     a = dict(shards=[f() for _ in range(R)], R=R, T=T, stride=stride, Q=Q, K=K, wq=f(), wk=f(),
-             q_out=f(), ldq=R * Q if ldq is None else ldq, k_out=f(), ldk=R * K if ldk is None else ldk)
+             q_out=f(), ldq=R * Q if ldq is None else ldq, k_out=f(), ldk=R * K if ldk is None else ldk,
+             flags=flags)
     if mutate:
         mutate(a)
     arr = None if a["shards"] is None else (ctypes.c_void_p * len(a["shards"]))(*a["shards"])
     st = lib.ts_qk_norm_sharded(arr, a["R"], a["T"], a["stride"], a["Q"], a["K"], a["wq"], a["wk"], 1e-6,
-                                a["q_out"], a["ldq"], a["k_out"], a["ldk"], None)
+                                a["q_out"], a["ldq"], a["k_out"], a["ldk"], a["flags"], None)
+    return st, lib.ts_last_error_detail().decode()
+
+
+def _rms_call(lib, R=8, T=4, stride=768, W=768, ldo=None, flags=0, mutate=None):
+    f = Fake()
+    a = dict(shards=[f() for _ in range(R)], R=R, T=T, stride=stride, W=W, w=f(), out=f(),
+             ldo=R * W if ldo is None else ldo, flags=flags)
+    if mutate:
+        mutate(a)
+    arr = None if a["shards"] is None else (ctypes.c_void_p * len(a["shards"]))(*a["shards"])
+    st = lib.ts_rms_norm_sharded(arr, a["R"], a["T"], a["stride"], a["W"], a["w"], 1e-6, a["out"], a["ldo"],
+                                 a["flags"], None)
     return st, lib.ts_last_error_detail().decode()
 
 
@@ -228,6 +241,8 @@ NEG_QK = [
     ("q_out overlaps k_out", dict(mutate=lambda a: a.update(k_out=a["q_out"] + 64)), ALIAS),
     ("q_out overlaps a shard", dict(mutate=lambda a: a.update(q_out=a["shards"][2] + 1024)), ALIAS),
     ("k_out overlaps wk", dict(mutate=lambda a: a.update(k_out=a["wk"])), ALIAS),
+    ("K 0 (use the single-matrix call)", dict(K=0), SHAPE),
+    ("unknown flag", dict(flags=4), UNSUPPORTED),
 ]
 
 
@@ -244,3 +259,37 @@ def test_binding_requires_cuda_tensors():
     x = torch.zeros(4, 64, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         pkg.ts_fused_reduce_norm(0, [x], allreduce_out=x)
+
+
+def test_rms_zero_tokens_is_valid(lib):
+    assert _rms_call(lib, T=0)[0] == TS_OK
+    assert _rms_call(lib, T=0, mutate=lambda a: a.update(shards=[None] * 8, out=None))[0] == TS_OK
+
+
+NEG_RMS = [
+    ("shards NULL", dict(mutate=lambda a: a.update(shards=None)), NULL),
+    ("R 0", dict(mutate=lambda a: a.update(R=0)), SHAPE),
+    ("W % 8", dict(W=100, stride=104), SHAPE),
+    ("W too big", dict(W=4104, stride=4104), UNSUPPORTED),
+    ("stride < W", dict(stride=760), SHAPE),
+    ("ldo small", dict(ldo=768 * 8 - 8), SHAPE),
+    ("weight NULL", dict(mutate=lambda a: a.update(w=None)), NULL),
+    ("out NULL", dict(mutate=lambda a: a.update(out=None)), NULL),
+    ("out misaligned", dict(mutate=lambda a: a.update(out=a["out"] + 2)), ALIGN),
+    ("out overlaps a shard", dict(mutate=lambda a: a.update(out=a["shards"][0])), ALIAS),
+    ("out overlaps weight", dict(mutate=lambda a: a.update(out=a["w"] - 64)), ALIAS),
+    ("unknown flag", dict(flags=8), UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", NEG_RMS, ids=[c[0] for c in NEG_RMS])
+def test_rms_rejects(lib, name, kw, want):
+    st, detail = _rms_call(lib, **kw)
+    assert st == want, (name, st, detail)
+    assert detail
+
+
+def test_pdl_flag_accepted(lib):
+    assert _fused_call(lib, T=0, flags=1)[0] == TS_OK
+    assert _qk_call(lib, T=0, flags=1)[0] == TS_OK
+    assert _rms_call(lib, T=0, flags=1)[0] == TS_OK

@@ -41,14 +41,26 @@ def _inputs(R, T, H, seed, p_std=1.0, outliers=0.0):
     return wl.fused_inputs(wl.FusedShape(R=R, T=T, H=H, p_std=p_std, outlier_frac=outliers), seed=seed)
 
 
-def _run_gpu(dev, pattern, inp, scale=None, P=0, swizzled=False, allreduce=True, stream=None):
+LIN, SW128, SW8 = pkg.SFLayout.LINEAR, pkg.SFLayout.SWIZZLED_128x4, pkg.SFLayout.SWIZZLED_8x4
+
+
+def _swizzle(layout, sf_linear):
+    return oracle.sf_swizzle_128x4(sf_linear) if layout == SW128 else oracle.sf_swizzle_8x4(sf_linear)
+
+
+def _sf_offset(layout, m, k, n_sf):
+    if layout == SW128:
+        return oracle.sf_offset_swizzled_128x4(m, k, n_sf)
+    return oracle.sf_offset_swizzled_8x4(m, k, n_sf)
+
+
+def _run_gpu(dev, pattern, inp, scale=None, P=0, layout=LIN, allreduce=True, stream=None):
     parts = inp["partials"].to(dev)
     res = inp["residual"].to(dev)
     gamma = inp["gamma"].to(dev)
     T, H = res.shape
-    g = guarded_outputs(pattern, T, H, dev, P, swizzled, allreduce)
+    g = guarded_outputs(pattern, T, H, dev, P, int(layout), allreduce)
     sf = None if scale is None else torch.tensor([scale], dtype=torch.float32, device=dev)
-    layout = pkg.SFLayout.SWIZZLED_128x4 if swizzled else pkg.SFLayout.LINEAR
     pkg.ts_fused_reduce_norm(pattern, parts, None if pattern == 0 else res, None if pattern == 0 else gamma,
                              EPS, sf, sf_layout=layout, stream=stream, **{k: v.t for k, v in g.items()})
     torch.cuda.synchronize()
@@ -62,7 +74,7 @@ def _oracle(pattern, inp, scale=0.0, P=0, rows=None):
                                     wl.bits(inp["gamma"]), EPS, scale, P, rows=rows)
 
 
-def _compare(pattern, got, want, swizzled=False, T=None, rows=None):
+def _compare(pattern, got, want, layout=LIN, T=None, rows=None):
     """got: full GPU outputs; want: oracle outputs on ``rows`` (all by default)."""
     sel = (lambda a: a) if rows is None else (lambda a: a[rows])
     assert np.array_equal(sel(got["allreduce_out"]), want["allreduce_out"]), "allreduce_out"
@@ -84,13 +96,13 @@ def _compare(pattern, got, want, swizzled=False, T=None, rows=None):
         codes_close(e2m1_nibbles(sel(got["quant_out"])), e2m1_nibbles(want["quant_out"]), e2m1_order, 1,
                     1e-4, "e2m1 codes")
         sf = got["scale_out"]
-        if swizzled:
+        if layout != LIN:
             lin = np.zeros_like(want["sf_out"])
             full_rows = np.arange(T) if rows is None else rows
             n_sf = want["sf_out"].shape[1]
             flat = sf.reshape(-1)
             for i, m in enumerate(full_rows):
-                offs = [oracle.sf_offset_swizzled_128x4(int(m), k, n_sf) for k in range(n_sf)]
+                offs = [_sf_offset(layout, int(m), k, n_sf) for k in range(n_sf)]
                 lin[i] = flat[offs]
             codes_close(lin, want["sf_out"], e4m3_order, 1, 1e-4, "SF (swizzled)")
         else:
@@ -161,15 +173,15 @@ def test_small_shapes(dev, pattern, R, T, H):
     base = _run_gpu(dev, 1, inp)
     amax = float(np.abs(f32_of_bf16(base["norm_out"])).max())
     scale = {2: 448.0 / amax, 4: 448.0 / amax, 3: 2688.0 / amax, 5: 2688.0 / amax}.get(pattern)
-    for swz in ((False, True) if pattern in (3, 5) else (False,)):
-        got = _run_gpu(dev, pattern, inp, scale, P, swz)
+    for layout in ((LIN, SW128, SW8) if pattern in (3, 5) else (LIN,)):
+        got = _run_gpu(dev, pattern, inp, scale, P, layout)
         want = _oracle(pattern, inp, scale or 0.0, P)
-        _compare(pattern, got, want, swz, T)
+        _compare(pattern, got, want, layout, T)
         if pattern in (2, 3, 4, 5, 6, 7):
             got["norm_ref"] = base["norm_out"]
             sf = _self_consistency(pattern, got, scale)
-            if swz:
-                assert np.array_equal(got["scale_out"].reshape(-1), oracle.sf_swizzle_128x4(sf))
+            if layout != LIN:
+                assert np.array_equal(got["scale_out"].reshape(-1), _swizzle(layout, sf))
 
 
 def test_zero_rows(dev):
@@ -291,7 +303,7 @@ def _compare_rows(pattern, got, want, rows):
 
 @pytest.mark.slow
 def test_full_size_nvfp4(dev):
-    """NVFP4, R=4, T=16384, H=5120, SF in LINEAR and SWIZZLED_128x4."""
+    """NVFP4, R=4, T=16384, H=5120, SF in LINEAR, SWIZZLED_128x4 and SWIZZLED_8x4."""
     inp = wl.fused_inputs(wl.WORKLOADS["C4"], seed=0)
     base = _run_gpu(dev, 1, inp, allreduce=False)
     amax = float(np.abs(f32_of_bf16(base["norm_out"])).max())
@@ -305,6 +317,38 @@ def test_full_size_nvfp4(dev):
     codes_close(lin["scale_out"][rows], want["sf_out"], e4m3_order, 1, 1e-4, "SF")
     lin["norm_ref"] = base["norm_out"]
     sf = _self_consistency(3, lin, g)
-    swz = _run_gpu(dev, 3, inp, g, swizzled=True, allreduce=False)
-    assert np.array_equal(swz["quant_out"], lin["quant_out"])
-    assert np.array_equal(swz["scale_out"].reshape(-1), oracle.sf_swizzle_128x4(sf))
+    for layout in (SW128, SW8):
+        swz = _run_gpu(dev, 3, inp, g, layout=layout, allreduce=False)
+        assert np.array_equal(swz["quant_out"], lin["quant_out"])
+        assert np.array_equal(swz["scale_out"].reshape(-1), _swizzle(layout, sf))
+
+
+def test_pdl_dependent_chain_matches_plain(dev):
+    """Six calls where each reads the previous call's residual_out: with the
+    PDL flag every launch must still see its predecessor's writes."""
+    inp = _inputs(8, 512, 7168, seed=11)
+    parts = inp["partials"].to(dev)
+    gamma = inp["gamma"].to(dev)
+
+    def chain(pdl, pattern):
+        res = inp["residual"].to(dev).clone()
+        outs = []
+        for _ in range(6):
+            ro = torch.empty_like(res)
+            extra = {}
+            if pattern == 1:
+                extra["norm_out"] = torch.empty_like(res)
+            else:
+                extra["quant_out"] = torch.empty(res.shape, dtype=torch.uint8, device=dev)
+                extra["scale_out"] = torch.empty((res.shape[0], res.shape[1] // 128), dtype=torch.float32,
+                                                 device=dev)
+            pkg.ts_fused_reduce_norm(pattern, parts, res, gamma, EPS, residual_out=ro, launch_with_pdl=pdl,
+                                     **extra)
+            res = ro
+            outs += list(extra.values())
+        torch.cuda.synchronize()
+        return [host(o) for o in outs] + [host(res)]
+
+    for pattern in (1, 6):
+        for x, y in zip(chain(False, pattern), chain(True, pattern)):
+            assert np.array_equal(x, y)

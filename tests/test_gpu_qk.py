@@ -107,3 +107,64 @@ def test_full_size_minimax(dev):
     wq, wk = _oracle(inp, 1024, 128, rows=rows)
     assert_bf16_close(q[rows], wq, 1, 0.999, "q_out")
     assert_bf16_close(k[rows], wk, 1, 0.999, "k_out")
+
+
+# ---------------------------------------------------------------------------
+# single-matrix sharded RMSNorm (ts_rms_norm_sharded)
+# ---------------------------------------------------------------------------
+
+def _rms_inputs(R, T, W, extra, seed):
+    g = torch.Generator().manual_seed(seed)
+    shards = torch.randn((R, T, W + extra), generator=g).to(torch.bfloat16)
+    w = (torch.rand(R * W, generator=g) + 0.5).to(torch.bfloat16)
+    return shards, w
+
+
+RMS_CASES = [(8, 33, 768, 0, 0), (1, 1, 8, 0, 0), (2, 9, 3072, 0, 0), (3, 17, 136, 24, 8),
+             (16, 5, 384, 64, 0), (5, 130, 4096, 8, 16), (4, 64, 1024, 0, 64)]
+
+
+@pytest.mark.parametrize("R,T,W,extra,pad", RMS_CASES, ids=[f"R{c[0]}-T{c[1]}-W{c[2]}" for c in RMS_CASES])
+def test_single_matrix_small_shapes(dev, R, T, W, extra, pad):
+    shards, w = _rms_inputs(R, T, W, extra, seed=R * 7 + T)
+    g = Guarded((T, R * W + pad), torch.bfloat16, dev)
+    pkg.ts_rms_norm_sharded(shards.to(dev), W, w.to(dev), EPS, out=g.t)
+    torch.cuda.synchronize()
+    assert g.intact()
+    out = host(g.t)
+    assert (out[:, R * W:] == np.uint16(FILL | (FILL << 8))).all()
+    want = oracle.rms_norm_sharded([wl.bits(s) for s in shards], W, wl.bits(w), EPS)
+    assert_bf16_close(out[:, :R * W], want, 1, 0.999, "single-matrix")
+
+
+def test_single_matrix_agrees_with_qk_q_segment(dev):
+    inp = wl.qk_inputs(wl.QKShape(R=8, T=64, q_shard=1024, k_shard=128, v_shard=128), seed=12)
+    sh = inp["shards"].to(dev)
+    q, _ = pkg.ts_qk_norm_sharded(sh, 1024, 128, inp["q_weight"].to(dev), inp["k_weight"].to(dev), EPS)
+    single = pkg.ts_rms_norm_sharded(sh, 1024, inp["q_weight"].to(dev), EPS)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(q), host(single))
+
+
+@pytest.mark.slow
+def test_single_matrix_full_size(dev):
+    """R=8 shards of [T=32768, 768] (MiniMax-M2's 6144-wide q split 8 ways)."""
+    shards, w = _rms_inputs(8, 32768, 768, 0, seed=0)
+    out = pkg.ts_rms_norm_sharded(shards.to(dev), 768, w.to(dev), EPS)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([np.arange(32), np.arange(32768 - 32, 32768), rng.integers(0, 32768, 2000)]))
+    want = oracle.rms_norm_sharded([wl.bits(s) for s in shards], 768, wl.bits(w), EPS, rows=rows)
+    assert_bf16_close(host(out)[rows], want, 1, 0.999, "single-matrix full size")
+
+
+def test_pdl_qk_matches_plain(dev):
+    inp = wl.qk_inputs(wl.QKShape(R=8, T=300, q_shard=1024, k_shard=128, v_shard=128), seed=13)
+    sh = inp["shards"].to(dev)
+    wq, wk = inp["q_weight"].to(dev), inp["k_weight"].to(dev)
+    a = pkg.ts_qk_norm_sharded(sh, 1024, 128, wq, wk, EPS)
+    b = pkg.ts_qk_norm_sharded(sh, 1024, 128, wq, wk, EPS, launch_with_pdl=True)
+    c = pkg.ts_rms_norm_sharded(sh, 1024, wq, EPS, launch_with_pdl=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(a[0]), host(b[0])) and np.array_equal(host(a[1]), host(b[1]))
+    assert np.array_equal(host(a[0]), host(c))
