@@ -100,6 +100,12 @@ def load(path: str | None = None):
             ctypes.c_float, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
             c_i64p, ctypes.c_int64, c_u16p, c_u16p, c_u16p, c_u16p, c_u8p, c_f32p, c_u8p]
         lib.orc_fused_reduce_norm_rows.restype = ctypes.c_int
+        lib.orc_rs_token_split.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, c_i64p, c_i64p]
+        lib.orc_rs_token_split.restype = None
+        lib.orc_reducescatter_fused_norm.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.POINTER(c_u16p), ctypes.c_int64, ctypes.c_int, c_u16p, c_u16p,
+            c_u16p, ctypes.c_float, ctypes.c_float, ctypes.c_int64, c_u16p, c_u16p, c_u16p, c_u8p, c_f32p, c_u8p]
+        lib.orc_reducescatter_fused_norm.restype = ctypes.c_int
         lib.orc_qk_norm_sharded_rows.argtypes = [
             ctypes.c_int, ctypes.POINTER(c_u16p), ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int64, c_u16p, c_u16p, ctypes.c_float, c_i64p, ctypes.c_int64,
@@ -317,4 +323,69 @@ def rms_norm_sharded(shards, width: int, weight, eps: float = 1e-6, rows=None) -
                                           _ptr(out, ctypes.c_uint16))
     if rc != 0:
         raise ValueError("oracle rejected the sharded RMSNorm arguments")
+    return out
+
+
+RS_PATTERNS = {
+    "kReduceScatter": 0,
+    "kRSResidualRMSNorm": 1,
+    "kRSResidualRMSNormFP8Quant": 2,
+    "kRSResidualRMSNormFP4Quant": 3,
+    "kRSResidualRMSNormOutFP8Quant": 4,
+    "kRSResidualRMSNormOutFP4Quant": 5,
+    "kRSResidualRMSNormFP8BlockWiseQuant": 6,
+    "kRSAddResidualRMSNormFP8BlockWiseQuant": 7,
+    "kRSAddResidualRMSNorm": 8,
+}
+
+
+def rs_token_split(T: int, world: int, rank: int) -> tuple[int, int]:
+    start, count = ctypes.c_int64(), ctypes.c_int64()
+    load().orc_rs_token_split(T, world, rank, ctypes.byref(start), ctypes.byref(count))
+    return start.value, count.value
+
+
+def reducescatter_fused_norm(rs_pattern: int, partials, rank: int, add_in=None, residual=None, gamma=None,
+                             eps: float = 1e-6, scale_factor: float = 0.0) -> dict:
+    """Rank ``rank``'s reduce-scatter fusion output, all R partials local.
+
+    ``partials``: R uint16 arrays [T, H]; ``add_in``/``residual``: uint16 [count, H]
+    for the rank's token slice; returns compact outputs ``reducescatter_out``,
+    ``residual_out``, ``norm_out``, ``quant_out``, ``block_scale_out``, ``sf_out``
+    (those the pattern defines) with ``count`` rows.
+    """
+    parts = [_u16(p) for p in partials]
+    R = len(parts)
+    T, H = parts[0].shape
+    start, count = rs_token_split(T, R, rank)
+    form = {7: 6, 8: 1}.get(rs_pattern, rs_pattern)
+    out = {"reducescatter_out": np.empty((count, H), np.uint16)}
+    if form != 0:
+        residual = _u16(residual)
+        gamma = _u16(gamma)
+        assert residual.shape == (count, H) and gamma.shape == (H,)
+        out["residual_out"] = np.empty((count, H), np.uint16)
+        out["norm_out"] = np.empty((count, H), np.uint16)
+    if rs_pattern in (7, 8):
+        add_in = _u16(add_in)
+        assert add_in.shape == (count, H)
+    else:
+        add_in = None
+    if form in (2, 4, 6):
+        out["quant_out"] = np.empty((count, H), np.uint8)
+    if form in (3, 5):
+        out["quant_out"] = np.empty((count, H // 2), np.uint8)
+        out["sf_out"] = np.empty((count, H // 16), np.uint8)
+    if form == 6:
+        out["block_scale_out"] = np.empty((count, H // 128), np.float32)
+    arr = (ctypes.POINTER(ctypes.c_uint16) * R)(*[_ptr(p, ctypes.c_uint16) for p in parts])
+    g = lambda k, ct: _ptr(out.get(k), ct)  # noqa: E731
+    rc = load().orc_reducescatter_fused_norm(
+        int(rs_pattern), R, arr, T, int(rank), _ptr(add_in, ctypes.c_uint16), _ptr(residual, ctypes.c_uint16),
+        _ptr(gamma, ctypes.c_uint16), float(eps), float(scale_factor), H,
+        g("reducescatter_out", ctypes.c_uint16), g("residual_out", ctypes.c_uint16),
+        g("norm_out", ctypes.c_uint16), g("quant_out", ctypes.c_uint8), g("block_scale_out", ctypes.c_float),
+        g("sf_out", ctypes.c_uint8))
+    if rc != 0:
+        raise ValueError("oracle rejected the reduce-scatter arguments")
     return out

@@ -315,13 +315,17 @@ enum {
  *   scale    = rsqrt(variance + eps)
  *   norm     = x * scale * weight
  * and [P2] `amd_all_reduce_kernel` for kAllReduce (the sum alone). */
-int orc_fused_reduce_norm_rows(int pattern, int R, const uint16_t *const *partials,
-                               const uint16_t *residual, const uint16_t *gamma, float eps,
-                               float scale_factor, int64_t H, int64_t partial_cols,
-                               const int64_t *rows, int64_t nrows, uint16_t *allreduce_out,
-                               uint16_t *residual_out, uint16_t *norm_out,
-                               uint16_t *partial_norm_out, uint8_t *quant_out,
-                               float *block_scale_out, uint8_t *sf_out)
+/* The row pipeline shared by the all-reduce and reduce-scatter forms.  The
+ * partials are indexed by the listed row; residual and add_in (NULL = none)
+ * by the listed row minus local_row0 (0 for the all-reduce form; the first
+ * row of the rank's token slice for the reduce-scatter form). */
+static int fused_rows_core(int pattern, int R, const uint16_t *const *partials,
+                           const uint16_t *add_in, const uint16_t *residual, int64_t local_row0,
+                           const uint16_t *gamma, float eps, float scale_factor, int64_t H,
+                           int64_t partial_cols, const int64_t *rows, int64_t nrows,
+                           uint16_t *allreduce_out, uint16_t *residual_out, uint16_t *norm_out,
+                           uint16_t *partial_norm_out, uint8_t *quant_out, float *block_scale_out,
+                           uint8_t *sf_out)
 {
     if (pattern < 0 || pattern > 8 || R < 1 || H < 1)
         return -1;
@@ -347,6 +351,7 @@ int orc_fused_reduce_norm_rows(int pattern, int R, const uint16_t *const *partia
     for (int64_t ri = 0; ri < nrows; ++ri) {
         const int64_t row = rows[ri];
         const int64_t in_off = row * H;
+        const int64_t loc_off = (row - local_row0) * H;
 
         /* reduce: fp32 accumulator starting at +0, peers in ascending order */
         for (int64_t j = 0; j < H; ++j) {
@@ -361,9 +366,14 @@ int orc_fused_reduce_norm_rows(int pattern, int R, const uint16_t *const *partia
         if (pattern == ORC_AR)
             continue;
 
+        /* the reduce-scatter "Add" operand, in fp32, before the residual */
+        if (add_in)
+            for (int64_t j = 0; j < H; ++j)
+                x[j] = x[j] + orc_bf16_decode(add_in[loc_off + j]);
+
         /* residual add, in fp32; residual_out is its bf16 rounding */
         for (int64_t j = 0; j < H; ++j)
-            x[j] = x[j] + orc_bf16_decode(residual[in_off + j]);
+            x[j] = x[j] + orc_bf16_decode(residual[loc_off + j]);
         if (residual_out)
             for (int64_t j = 0; j < H; ++j)
                 residual_out[ri * H + j] = orc_bf16_encode(x[j]);
@@ -434,6 +444,76 @@ int orc_fused_reduce_norm_rows(int pattern, int R, const uint16_t *const *partia
     free(x);
     free(n);
     return 0;
+}
+
+/* Row-wise evaluation of one AllReduceFusionPattern on the rows listed in
+ * rows[0..nrows).  Inputs: R partial tensors and the residual, bf16 [*, H]
+ * row-major (stride H); gamma bf16 [H].  Outputs are compact, one row per
+ * listed row (see fused_rows_core and the output list above).  Returns 0, or
+ * -1 on an unknown pattern / bad sizes. */
+int orc_fused_reduce_norm_rows(int pattern, int R, const uint16_t *const *partials,
+                               const uint16_t *residual, const uint16_t *gamma, float eps,
+                               float scale_factor, int64_t H, int64_t partial_cols,
+                               const int64_t *rows, int64_t nrows, uint16_t *allreduce_out,
+                               uint16_t *residual_out, uint16_t *norm_out,
+                               uint16_t *partial_norm_out, uint8_t *quant_out,
+                               float *block_scale_out, uint8_t *sf_out)
+{
+    return fused_rows_core(pattern, R, partials, NULL, residual, 0, gamma, eps, scale_factor, H,
+                           partial_cols, rows, nrows, allreduce_out, residual_out, norm_out,
+                           partial_norm_out, quant_out, block_scale_out, sf_out);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Reduce-scatter fusion restated for one GPU ([P1] `trtllm_reducescatter_  */
+/* fusion`, `ReduceScatterFusionPattern`; token split of [P2]               */
+/* `rsag_get_token_dist`).                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Token slice of rank `rank` among `world` ranks: T/world tokens each, the
+ * first T%world ranks one more, slices in rank order. */
+void orc_rs_token_split(int64_t T, int world, int rank, int64_t *start, int64_t *count)
+{
+    int64_t base = T / world, extra = T % world;
+    *count = base + (rank < extra ? 1 : 0);
+    *start = rank * base + (rank < extra ? rank : extra);
+}
+
+/* Rank `rank`'s output of the reduce-scatter fusion, all R partials local
+ * (world size = R).  partials: R bf16 [T, H] (every rank's contribution for
+ * all T tokens); add_in and residual: bf16 [count, H] for the rank's slice
+ * (add_in only for codes 7 and 8).  ReduceScatterFusionPattern codes:
+ *   0 kReduceScatter                          -> all-reduce form 0
+ *   1..6 kRSResidualRMSNorm...FP8BlockWise    -> all-reduce forms 1..6
+ *   7 kRSAddResidualRMSNormFP8BlockWiseQuant  -> form 6 with add_in
+ *   8 kRSAddResidualRMSNorm                   -> form 1 with add_in
+ * with x = ((sum of partials) + add_in) + residual, and reducescatter_out =
+ * bf16(sum of partials) (before add_in).  Outputs are compact [count, ...]. */
+int orc_reducescatter_fused_norm(int rs_pattern, int R, const uint16_t *const *partials, int64_t T,
+                                 int rank, const uint16_t *add_in, const uint16_t *residual,
+                                 const uint16_t *gamma, float eps, float scale_factor, int64_t H,
+                                 uint16_t *reducescatter_out, uint16_t *residual_out,
+                                 uint16_t *norm_out, uint8_t *quant_out, float *block_scale_out,
+                                 uint8_t *sf_out)
+{
+    if (rs_pattern < 0 || rs_pattern > 8 || R < 1 || rank < 0 || rank >= R || T < 0)
+        return -1;
+    const int with_add = (rs_pattern == 7 || rs_pattern == 8);
+    const int form = rs_pattern == 7 ? ORC_AR_RES_RMS_FP8_BLOCK : (rs_pattern == 8 ? ORC_AR_RES_RMS : rs_pattern);
+    if (with_add && !add_in)
+        return -1;
+    int64_t start, count;
+    orc_rs_token_split(T, R, rank, &start, &count);
+    int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)(count > 0 ? count : 1));
+    if (!rows)
+        return -1;
+    for (int64_t i = 0; i < count; ++i)
+        rows[i] = start + i;
+    int rc = fused_rows_core(form, R, partials, with_add ? add_in : NULL, residual, start, gamma, eps,
+                             scale_factor, H, 0, rows, count, reducescatter_out, residual_out,
+                             norm_out, NULL, quant_out, block_scale_out, sf_out);
+    free(rows);
+    return rc;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -16,8 +16,14 @@ SRC = os.path.join(ROOT, "oracle", "oracle.c")
 MUTANTS = {
     "drop_first_partial": ("acc = acc + orc_bf16_decode(partials[r][in_off + j]);",
                            "acc = acc + (r ? orc_bf16_decode(partials[r][in_off + j]) : 0.0f);"),
-    "residual_sign": ("x[j] = x[j] + orc_bf16_decode(residual[in_off + j]);",
-                      "x[j] = x[j] - orc_bf16_decode(residual[in_off + j]);"),
+    "residual_sign": ("x[j] = x[j] + orc_bf16_decode(residual[loc_off + j]);",
+                      "x[j] = x[j] - orc_bf16_decode(residual[loc_off + j]);"),
+    "add_in_sign": ("x[j] = x[j] + orc_bf16_decode(add_in[loc_off + j]);",
+                    "x[j] = x[j] - orc_bf16_decode(add_in[loc_off + j]);"),
+    "add_in_wrong_row": ("x[j] = x[j] + orc_bf16_decode(add_in[loc_off + j]);",
+                         "x[j] = x[j] + orc_bf16_decode(add_in[in_off + j]);"),
+    "token_split_extra_to_last": ("*count = base + (rank < extra ? 1 : 0);",
+                                  "*count = base + (rank >= world - extra ? 1 : 0);"),
     "mean_over_h_minus_1": ("float variance = (float)(ss / (double)H);",
                             "float variance = (float)(ss / (double)(H - 1));"),
     "eps_dropped": ("float t = variance + eps;", "float t = variance;"),
@@ -58,6 +64,6 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env = dict(os.environ, ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "tests/test_oracle_formats.py", "tests/test_oracle_fused.py",
-                        "tests/test_oracle_qk.py"], cwd=ROOT, env=env, capture_output=True,
+                        "tests/test_oracle_qk.py", "tests/test_oracle_rs.py"], cwd=ROOT, env=env, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 1, f"no pin caught mutant {name}:\n{r.stdout[-2000:]}"
