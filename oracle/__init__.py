@@ -106,6 +106,11 @@ def load(path: str | None = None):
             ctypes.c_int, ctypes.c_int, ctypes.POINTER(c_u16p), ctypes.c_int64, ctypes.c_int, c_u16p, c_u16p,
             c_u16p, ctypes.c_float, ctypes.c_float, ctypes.c_int64, c_u16p, c_u16p, c_u16p, c_u8p, c_f32p, c_u8p]
         lib.orc_reducescatter_fused_norm.restype = ctypes.c_int
+        lib.orc_allgather_fused_norm_rows.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.POINTER(c_u16p), ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64, c_u16p, c_u16p, ctypes.c_float, ctypes.c_float, c_i64p, ctypes.c_int64, c_u16p,
+            c_u16p, c_u16p, c_u8p, c_f32p]
+        lib.orc_allgather_fused_norm_rows.restype = ctypes.c_int
         lib.orc_qk_norm_sharded_rows.argtypes = [
             ctypes.c_int, ctypes.POINTER(c_u16p), ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int64, c_u16p, c_u16p, ctypes.c_float, c_i64p, ctypes.c_int64,
@@ -388,4 +393,46 @@ def reducescatter_fused_norm(rs_pattern: int, partials, rank: int, add_in=None, 
         g("sf_out", ctypes.c_uint8))
     if rc != 0:
         raise ValueError("oracle rejected the reduce-scatter arguments")
+    return out
+
+
+AG_PATTERNS = {"kAllGather": 0, "kAllGatherfusedRMS": 1, "kAllGatherfusedRMSFP8BlockWiseQuant": 2}
+
+
+def allgather_fused_norm(pattern: int, inputs, q_lora_rank: int, kv_lora_rank: int, x_gamma=None, y_gamma=None,
+                         x_eps: float = 1e-6, y_eps: float = 1e-6, rows=None) -> dict:
+    """All-gather fusion with the dual MLA RMSNorm on the listed gathered rows.
+
+    ``inputs``: R uint16 arrays [count_r, hidden] (rank r's token slice, the
+    counts of ``rs_token_split``).  Returns compact ``allgather_out`` [n, hidden]
+    and, by pattern, ``x_norm_out`` [n, q], ``y_norm_out`` [n, kv], ``quant_out``
+    uint8 [n, q], ``scale_out`` float32 [n, q/128].
+    """
+    ins = [_u16(x) for x in inputs]
+    R = len(ins)
+    hidden = ins[0].shape[1]
+    T = sum(x.shape[0] for x in ins)
+    for r, x in enumerate(ins):
+        assert x.shape == (rs_token_split(T, R, r)[1], hidden)
+    rows = np.arange(T, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.size
+    q, kv = q_lora_rank, kv_lora_rank
+    out = {"allgather_out": np.empty((n, hidden), np.uint16)}
+    if pattern in (1, 2):
+        x_gamma, y_gamma = _u16(x_gamma), _u16(y_gamma)
+        assert x_gamma.shape == (q,) and y_gamma.shape == (kv,)
+        out["x_norm_out"] = np.empty((n, q), np.uint16)
+        out["y_norm_out"] = np.empty((n, kv), np.uint16)
+    if pattern == 2:
+        out["quant_out"] = np.empty((n, q), np.uint8)
+        out["scale_out"] = np.empty((n, q // 128), np.float32)
+    arr = (ctypes.POINTER(ctypes.c_uint16) * R)(*[_ptr(x, ctypes.c_uint16) for x in ins])
+    g = lambda k, ct: _ptr(out.get(k), ct)  # noqa: E731
+    rc = load().orc_allgather_fused_norm_rows(
+        int(pattern), R, arr, T, hidden, q, kv, _ptr(x_gamma, ctypes.c_uint16), _ptr(y_gamma, ctypes.c_uint16),
+        float(x_eps), float(y_eps), _ptr(rows, ctypes.c_int64), n, g("allgather_out", ctypes.c_uint16),
+        g("x_norm_out", ctypes.c_uint16), g("y_norm_out", ctypes.c_uint16), g("quant_out", ctypes.c_uint8),
+        g("scale_out", ctypes.c_float))
+    if rc != 0:
+        raise ValueError("oracle rejected the all-gather arguments")
     return out

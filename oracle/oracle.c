@@ -615,3 +615,99 @@ int orc_rms_norm_sharded_rows(int R, const uint16_t *const *shards, int64_t row_
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* All-gather fusion with the dual RMSNorm of MLA segments, restated for one */
+/* GPU ([P1] `trtllm_allgather_fusion`, `AllGatherFusionPattern`).          */
+/* ------------------------------------------------------------------------ */
+
+/* RMSNorm of one segment of a row: n_j = bf16((v_j * rsqrt(mean(v^2) + eps)) * w_j),
+ * mean in double rounded to fp32, rsqrt correctly rounded; nf receives the
+ * bf16-rounded values widened back to fp32. */
+static void segment_rmsnorm(const uint16_t *v, int64_t width, const uint16_t *w, float eps,
+                            uint16_t *out, float *nf)
+{
+    double ss = 0.0;
+    for (int64_t j = 0; j < width; ++j) {
+        double d = orc_bf16_decode(v[j]);
+        ss += d * d;
+    }
+    float var = (float)(ss / (double)width);
+    float s = (float)(1.0 / sqrt((double)(var + eps)));
+    for (int64_t j = 0; j < width; ++j) {
+        uint16_t b = orc_bf16_encode((orc_bf16_decode(v[j]) * s) * orc_bf16_decode(w[j]));
+        if (out)
+            out[j] = b;
+        nf[j] = orc_bf16_decode(b);
+    }
+}
+
+/* The gathered token rows [T, hidden] are the R ranks' slices in rank order
+ * (rank r holds T/R tokens, the first T%R ranks one more: [P2]
+ * `rsag_get_token_dist`); inputs[r] is rank r's [count_r, hidden] slice.
+ * Each row is x (q_lora_rank columns) | y (kv_lora_rank) | rope (the rest).
+ *   pattern 0 kAllGather                       allgather_out only
+ *   pattern 1 kAllGatherfusedRMS               + x_norm_out [T, q], y_norm_out [T, kv]
+ *   pattern 2 kAllGatherfusedRMSFP8BlockWiseQuant
+ *             + y_norm_out, and the x norm as FP8 1x128 blocks: quant_out
+ *             e4m3 [T, q], scale_out fp32 [T, q/128] (s = amax/448, code =
+ *             e4m3(n/s), 0 for an all-zero block); x_norm_out optional.
+ * Each norm is its own RMSNorm over its segment with its gamma and eps.
+ * Outputs are compact, one row per listed gathered row.  Returns 0 or -1. */
+int orc_allgather_fused_norm_rows(int pattern, int R, const uint16_t *const *inputs, int64_t T,
+                                  int64_t hidden, int64_t q, int64_t kv, const uint16_t *x_gamma,
+                                  const uint16_t *y_gamma, float x_eps, float y_eps, const int64_t *rows,
+                                  int64_t nrows, uint16_t *allgather_out, uint16_t *x_norm_out,
+                                  uint16_t *y_norm_out, uint8_t *quant_out, float *scale_out)
+{
+    if (pattern < 0 || pattern > 2 || R < 1 || q < 1 || kv < 1 || q + kv > hidden)
+        return -1;
+    if (pattern == 2 && q % ORC_FP8_BLOCK)
+        return -1;
+    float *nx = (float *)malloc(sizeof(float) * (size_t)q);
+    float *ny = (float *)malloc(sizeof(float) * (size_t)kv);
+    if (!nx || !ny) {
+        free(nx);
+        free(ny);
+        return -1;
+    }
+    for (int64_t ri = 0; ri < nrows; ++ri) {
+        const int64_t t = rows[ri];
+        /* which rank's slice holds gathered row t */
+        int rank = 0;
+        int64_t start = 0, count = 0;
+        for (int r = 0; r < R; ++r) {
+            orc_rs_token_split(T, R, r, &start, &count);
+            if (t >= start && t < start + count) {
+                rank = r;
+                break;
+            }
+        }
+        const uint16_t *row = inputs[rank] + (t - start) * hidden;
+        if (allgather_out)
+            for (int64_t j = 0; j < hidden; ++j)
+                allgather_out[ri * hidden + j] = row[j];
+        if (pattern == 0)
+            continue;
+        segment_rmsnorm(row, q, x_gamma, x_eps, x_norm_out ? x_norm_out + ri * q : NULL, nx);
+        segment_rmsnorm(row + q, kv, y_gamma, y_eps, y_norm_out ? y_norm_out + ri * kv : NULL, ny);
+        if (pattern == 2) {
+            const int64_t G = q / ORC_FP8_BLOCK;
+            for (int64_t g = 0; g < G; ++g) {
+                float amax = 0.0f;
+                for (int64_t j = g * ORC_FP8_BLOCK; j < (g + 1) * ORC_FP8_BLOCK; ++j)
+                    if (fabsf(nx[j]) > amax)
+                        amax = fabsf(nx[j]);
+                float s = amax / 448.0f;
+                if (scale_out)
+                    scale_out[ri * G + g] = s;
+                if (quant_out)
+                    for (int64_t j = g * ORC_FP8_BLOCK; j < (g + 1) * ORC_FP8_BLOCK; ++j)
+                        quant_out[ri * q + j] = (s == 0.0f) ? 0 : orc_e4m3_encode(nx[j] / s);
+            }
+        }
+    }
+    free(nx);
+    free(ny);
+    return 0;
+}

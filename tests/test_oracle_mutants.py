@@ -45,6 +45,11 @@ MUTANTS = {
     "single_matrix_no_div_r": ("(double)(V / (float)R + eps)", "(double)(V + eps)"),
     "single_matrix_weight_slice": ("orc_bf16_decode(weight[r * W + j])", "orc_bf16_decode(weight[j])"),
     "swizzle8_row_stride": ("return tile * 32 + (m % 8) * 4 + (k % 4);", "return tile * 32 + (m % 8) * 3 + (k % 4);"),
+    "ag_y_uses_x_eps": ("segment_rmsnorm(row + q, kv, y_gamma, y_eps,", "segment_rmsnorm(row + q, kv, y_gamma, x_eps,"),
+    "ag_y_uses_x_gamma": ("segment_rmsnorm(row + q, kv, y_gamma,", "segment_rmsnorm(row + q, kv, x_gamma,"),
+    # (an earlier rank's slice never has fewer rows, so the planted read stays in bounds)
+    "ag_wrong_rank": ("const uint16_t *row = inputs[rank] + (t - start) * hidden;",
+                      "const uint16_t *row = inputs[rank > 0 ? rank - 1 : 0] + (t - start) * hidden;"),
     "swizzle_rows_cols": ("return tile * 512 + j * 16 + i * 4 + (k % 4);",
                           "return tile * 512 + i * 16 + j * 4 + (k % 4);"),
 }
@@ -64,6 +69,6 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env = dict(os.environ, ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "tests/test_oracle_formats.py", "tests/test_oracle_fused.py",
-                        "tests/test_oracle_qk.py", "tests/test_oracle_rs.py"], cwd=ROOT, env=env, capture_output=True,
+                        "tests/test_oracle_qk.py", "tests/test_oracle_rs.py", "tests/test_oracle_ag.py"], cwd=ROOT, env=env, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 1, f"no pin caught mutant {name}:\n{r.stdout[-2000:]}"
