@@ -84,6 +84,26 @@ def qk_bytes(R: int, T: int, Q: int, K: int) -> int:
     return T * R * (Q + K) * 2 * 2 + R * (Q + K) * 2
 
 
+def rs_add_bytes(R: int, T: int, H: int, fp8_block: bool = False) -> int:
+    """kRSAddResidualRMSNorm(FP8BlockWise) over all R ranks' slices (R calls):
+    the partials' rows, add_in, residual, gamma once per call, and the outputs."""
+    rb = T * R * H * 2 + 2 * T * H * 2 + R * H * 2
+    wb = T * H * 2 + (T * H + T * (H // 128) * 4 if fp8_block else T * H * 2)
+    return rb + wb
+
+
+def ag_bytes(pattern: int, T: int, q: int, kv: int, rope: int) -> int:
+    """All-gather dual norm: read every row once, write the gathered copy and the
+    pattern's outputs (pattern 2 here without the optional bf16 x norm)."""
+    hidden = q + kv + rope
+    b = T * hidden * 2 * 2
+    if pattern == 1:
+        b += T * (q + kv) * 2 + (q + kv) * 2
+    elif pattern == 2:
+        b += T * kv * 2 + T * q + T * (q // 128) * 4 + (q + kv) * 2
+    return b
+
+
 def rms_sharded_bytes(R: int, T: int, W: int) -> int:
     return T * R * W * 2 * 2 + R * W * 2
 
@@ -363,6 +383,50 @@ def _case_builders():
             return call, fused_bytes(3, 4, T, H, sf_layout=int(layout))
         return build
 
+    def rs_add(rs_pattern):
+        def build(dev, stream):
+            shape = wl.WORKLOADS["C3"]
+            inp = wl.fused_inputs(shape, seed=0, device=dev)
+            R, T, H = shape.R, shape.T, shape.H
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(1)
+            add = torch.randn((T, H), generator=gen, device=dev).to(torch.bfloat16)
+            calls = []
+            for rank in range(R):
+                start, count = pkg.rs_token_split(T, R, rank)
+                form = 6 if rs_pattern == 7 else 1
+                outs = pkg.new_outputs(form, count, H, dev)
+                calls.append((rank, add[start:start + count], inp["residual"][start:start + count], outs))
+
+            def call():
+                for rank, a_in, res, outs in calls:
+                    pkg.ts_reducescatter_fused_norm(rs_pattern, inp["partials"], rank, a_in, res, inp["gamma"],
+                                                    EPS, launch_with_pdl=True, stream=stream, **outs)
+            return call, rs_add_bytes(R, T, H, rs_pattern == 7)
+        return build
+
+    def ag(pattern):
+        def build(dev, stream):
+            R, T, q, kv, rope = 8, 65536, 1536, 512, 64
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(0)
+            full = torch.randn((T, q + kv + rope), generator=gen, device=dev).to(torch.bfloat16)
+            slices = [full[s:s + c].clone() for s, c in (pkg.rs_token_split(T, R, r) for r in range(R))]
+            del full
+            xg = (torch.rand(q, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
+            yg = (torch.rand(kv, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
+            e = lambda *sh, dt=torch.bfloat16: torch.empty(sh, dtype=dt, device=dev)  # noqa: E731
+            outs = {"allgather_out": e(T, q + kv + rope)}
+            if pattern == 1:
+                outs.update(x_norm_out=e(T, q), y_norm_out=e(T, kv))
+            elif pattern == 2:
+                outs.update(y_norm_out=e(T, kv), quant_out=e(T, q, dt=torch.uint8),
+                            scale_out=e(T, q // 128, dt=torch.float32))
+            call = lambda: pkg.ts_allgather_fused_norm(pattern, slices, q, kv, rope, xg, yg, EPS, EPS,  # noqa
+                                                       stream=stream, **outs)
+            return call, ag_bytes(pattern, T, q, kv, rope)
+        return build
+
     def c5(dev, stream):
         qs = wl.WORKLOADS["C5"]
         qi = wl.qk_inputs(qs, seed=0, device=dev)
@@ -400,6 +464,11 @@ def _case_builders():
         "c4-p3-linear": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF LINEAR", c4(2)),
         "c4-p3-swizzled": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF SWIZZLED_128x4", c4(0)),
         "c4-p3-swizzled8": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF SWIZZLED_8x4", c4(1)),
+        "rs-add": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls)", rs_add(8)),
+        "rs-add-fp8b": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls)",
+                        rs_add(7)),
+        "ag-rms": ("kAllGatherfusedRMS R=8 T=65536 1536|512|64", ag(1)),
+        "ag-rms-fp8b": ("kAllGatherfusedRMSFP8BlockWiseQuant R=8 T=65536 1536|512|64", ag(2)),
         "c5-qk": ("MiniMax QK-RMSNorm R=8 T=32768 Q=1024 K=128", c5),
         "single-768": ("single-matrix sharded RMSNorm R=8 T=32768 W=768", single),
         "c1-p1": ("kARResidualRMSNorm R=2 T=16 H=4096 (latency)", c1),

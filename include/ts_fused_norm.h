@@ -186,6 +186,93 @@ TS_API int ts_fused_reduce_norm(int pattern, const void *const *partials, int R,
                                 const void *gamma, float eps, const float *scale_factor, int64_t T,
                                 int64_t H, const ts_outs_t *outs, uint32_t flags, void *stream);
 
+/* Codes identical to `ReduceScatterFusionPattern` (tokenspeed trtllm.py). */
+typedef enum {
+    TS_RS = 0,                              /* kReduceScatter                           */
+    TS_RS_RES_RMS = 1,                      /* kRSResidualRMSNorm                       */
+    TS_RS_RES_RMS_FP8 = 2,                  /* kRSResidualRMSNormFP8Quant               */
+    TS_RS_RES_RMS_FP4 = 3,                  /* kRSResidualRMSNormFP4Quant               */
+    TS_RS_RES_RMS_OUT_FP8 = 4,              /* kRSResidualRMSNormOutFP8Quant            */
+    TS_RS_RES_RMS_OUT_FP4 = 5,              /* kRSResidualRMSNormOutFP4Quant            */
+    TS_RS_RES_RMS_FP8_BLOCKWISE = 6,        /* kRSResidualRMSNormFP8BlockWiseQuant      */
+    TS_RS_ADD_RES_RMS_FP8_BLOCKWISE = 7,    /* kRSAddResidualRMSNormFP8BlockWiseQuant   */
+    TS_RS_ADD_RES_RMS = 8                   /* kRSAddResidualRMSNorm                    */
+} ts_rs_pattern_t;
+
+/*
+ * ts_reducescatter_fused_norm: one rank's output of the reduce-scatter fusion
+ * (tokenspeed trtllm.py `trtllm_reducescatter_fusion`), with the R ranks'
+ * partials resident on this GPU (world size = R).  Rank `rank` owns the token
+ * slice [start, start + count) of tokenspeed triton.py `rsag_get_token_dist`:
+ * count = T/R, plus one for the first T%R ranks; slices in rank order.  Over
+ * that slice the call computes the all-reduce-form epilogue (the table of
+ * ts_outs_t, for the codes mapped below), with
+ *
+ *   x[i,j] = ((sum over r ascending of p_r[start+i, j]) + add_in[i,j]) + residual[i,j]
+ *
+ * (add_in only for codes 7 and 8), outs->allreduce_out playing the part of
+ * `reducescatter_out` = bf16(sum of the partials, before add_in).
+ *
+ *   rs_pattern    ts_rs_pattern_t.  0..6 behave as AllReduceFusionPattern
+ *                 0..6 on the slice; 7 = 6 with add_in; 8 = 1 with add_in.
+ *   partials      host array of R device pointers, each bf16 [T, H] (all T
+ *                 tokens; only the slice's rows are read).
+ *   rank          0..R-1.
+ *   add_in        bf16 [count, H]; required for codes 7 and 8, NULL otherwise.
+ *   residual      bf16 [count, H] (the slice's rows; codes 1..8).
+ *   outs          outputs with count rows (partial_norm_out must be NULL).
+ *   gamma, eps, scale_factor, H, flags, stream: as for ts_fused_reduce_norm.
+ * A rank whose slice is empty (T < R) validates and returns TS_OK.
+ */
+TS_API int ts_reducescatter_fused_norm(int rs_pattern, const void *const *partials, int R, int rank,
+                                       const void *add_in, const void *residual, const void *gamma,
+                                       float eps, const float *scale_factor, int64_t T, int64_t H,
+                                       const ts_outs_t *outs, uint32_t flags, void *stream);
+
+/* Codes identical to `AllGatherFusionPattern` (tokenspeed trtllm.py). */
+typedef enum {
+    TS_AG = 0,                      /* kAllGather                           */
+    TS_AG_RMS = 1,                  /* kAllGatherfusedRMS                   */
+    TS_AG_RMS_FP8_BLOCKWISE = 2     /* kAllGatherfusedRMSFP8BlockWiseQuant  */
+} ts_ag_pattern_t;
+
+/*
+ * ts_allgather_fused_norm: the all-gather fusion with the dual RMSNorm of MLA
+ * row segments (tokenspeed trtllm.py `trtllm_allgather_fusion`), with the R
+ * ranks' token slices resident on this GPU.  The gathered tensor is the
+ * slices in rank order (rank r holds T/R tokens, the first T%R ranks one
+ * more: tokenspeed triton.py `rsag_get_token_dist`).  Each gathered row is
+ * x (q_lora_rank columns) | y (kv_lora_rank) | rope (qk_rope_head_dim):
+ *
+ *   allgather_out[t, :] = the row                                  (all patterns)
+ *   x_norm_out[t, j]    = bf16((x_j * rsqrt(sum(x^2)/q + x_eps)) * x_gamma[j])
+ *   y_norm_out[t, j]    = bf16((y_j * rsqrt(sum(y^2)/kv + y_eps)) * y_gamma[j])
+ *   pattern 2: the x norm n in FP8 1x128 blocks: scale_out[t, g] = amax/448 (fp32),
+ *              quant_out[t, j] = e4m3(n_j / s) (0 for an all-zero block).
+ *   The rope columns only appear in allgather_out.
+ *
+ *   ag_pattern    ts_ag_pattern_t.
+ *   inputs        host array of R device pointers; inputs[r] is bf16
+ *                 [count_r, hidden] (may be NULL when count_r == 0).
+ *   T             gathered tokens, >= 0 (T == 0 returns TS_OK).
+ *   hidden        = q_lora_rank + kv_lora_rank + qk_rope_head_dim <= 2112.
+ *   q_lora_rank   positive multiple of 128; kv_lora_rank, qk_rope_head_dim
+ *                 multiples of 8 (kv > 0, rope >= 0).
+ *   x_gamma, y_gamma  bf16 [q_lora_rank], [kv_lora_rank] (patterns 1, 2).
+ *   outputs       allgather_out bf16 [T, hidden] (required); x_norm_out bf16
+ *                 [T, q] (required in 1, optional in 2, NULL in 0); y_norm_out
+ *                 bf16 [T, kv] (1, 2); quant_out e4m3 [T, q] and scale_out fp32
+ *                 [T, q/128] (2 only).  No output may overlap an input or
+ *                 another output.
+ *   flags, stream as for ts_fused_reduce_norm.
+ */
+TS_API int ts_allgather_fused_norm(int ag_pattern, const void *const *inputs, int R, int64_t T,
+                                   int64_t hidden, int64_t q_lora_rank, int64_t kv_lora_rank,
+                                   int64_t qk_rope_head_dim, const void *x_gamma, const void *y_gamma,
+                                   float x_eps, float y_eps, void *allgather_out, void *x_norm_out,
+                                   void *y_norm_out, void *quant_out, void *scale_out, uint32_t flags,
+                                   void *stream);
+
 /*
  * ts_qk_norm_sharded: MiniMax tensor-parallel QK-RMSNorm with the R shards
  * resident on this GPU (vLLM rms_norm_tp `_minimax_qk_norm_tp_eager`, split

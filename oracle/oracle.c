@@ -698,12 +698,12 @@ int orc_allgather_fused_norm_rows(int pattern, int R, const uint16_t *const *inp
                 for (int64_t j = g * ORC_FP8_BLOCK; j < (g + 1) * ORC_FP8_BLOCK; ++j)
                     if (fabsf(nx[j]) > amax)
                         amax = fabsf(nx[j]);
-                float s = amax / 448.0f;
+                float xs = amax / 448.0f;
                 if (scale_out)
-                    scale_out[ri * G + g] = s;
+                    scale_out[ri * G + g] = xs;
                 if (quant_out)
                     for (int64_t j = g * ORC_FP8_BLOCK; j < (g + 1) * ORC_FP8_BLOCK; ++j)
-                        quant_out[ri * q + j] = (s == 0.0f) ? 0 : orc_e4m3_encode(nx[j] / s);
+                        quant_out[ri * q + j] = (xs == 0.0f) ? 0 : orc_e4m3_encode(nx[j] / xs);
             }
         }
     }

@@ -34,6 +34,26 @@ class Pattern(enum.IntEnum):
     kARResidualRMSNormPartialOut = 8
 
 
+class RSPattern(enum.IntEnum):
+    """`ReduceScatterFusionPattern` codes (tokenspeed trtllm.py)."""
+    kReduceScatter = 0
+    kRSResidualRMSNorm = 1
+    kRSResidualRMSNormFP8Quant = 2
+    kRSResidualRMSNormFP4Quant = 3
+    kRSResidualRMSNormOutFP8Quant = 4
+    kRSResidualRMSNormOutFP4Quant = 5
+    kRSResidualRMSNormFP8BlockWiseQuant = 6
+    kRSAddResidualRMSNormFP8BlockWiseQuant = 7
+    kRSAddResidualRMSNorm = 8
+
+
+class AGPattern(enum.IntEnum):
+    """`AllGatherFusionPattern` codes (tokenspeed trtllm.py)."""
+    kAllGather = 0
+    kAllGatherfusedRMS = 1
+    kAllGatherfusedRMSFP8BlockWiseQuant = 2
+
+
 class SFLayout(enum.IntEnum):
     """`QuantizationSFLayout` codes (tokenspeed trtllm.py)."""
     SWIZZLED_128x4 = 0
@@ -63,8 +83,8 @@ class TsOuts(ctypes.Structure):
     ]
 
 
-EXPORTS = ("ts_fused_reduce_norm", "ts_qk_norm_sharded", "ts_rms_norm_sharded", "ts_status_string",
-           "ts_last_error_detail")
+EXPORTS = ("ts_fused_reduce_norm", "ts_reducescatter_fused_norm", "ts_allgather_fused_norm", "ts_qk_norm_sharded",
+           "ts_rms_norm_sharded", "ts_status_string", "ts_last_error_detail")
 
 TS_FLAG_PDL = 1
 
@@ -87,6 +107,14 @@ def library(path: str | None = None):
         lib.ts_fused_reduce_norm.argtypes = [ctypes.c_int, ctypes.POINTER(vp), ctypes.c_int, vp, vp,
                                              ctypes.c_float, vp, i64, i64, ctypes.POINTER(TsOuts), u32, vp]
         lib.ts_fused_reduce_norm.restype = ctypes.c_int
+        lib.ts_reducescatter_fused_norm.argtypes = [ctypes.c_int, ctypes.POINTER(vp), ctypes.c_int, ctypes.c_int,
+                                                    vp, vp, vp, ctypes.c_float, vp, i64, i64,
+                                                    ctypes.POINTER(TsOuts), u32, vp]
+        lib.ts_reducescatter_fused_norm.restype = ctypes.c_int
+        lib.ts_allgather_fused_norm.argtypes = [ctypes.c_int, ctypes.POINTER(vp), ctypes.c_int, i64, i64, i64, i64,
+                                                i64, vp, vp, ctypes.c_float, ctypes.c_float, vp, vp, vp, vp, vp,
+                                                u32, vp]
+        lib.ts_allgather_fused_norm.restype = ctypes.c_int
         lib.ts_qk_norm_sharded.argtypes = [ctypes.POINTER(vp), ctypes.c_int, i64, i64, i64, i64, vp, vp,
                                            ctypes.c_float, vp, i64, vp, i64, u32, vp]
         lib.ts_qk_norm_sharded.restype = ctypes.c_int
@@ -224,6 +252,88 @@ def ts_fused_reduce_norm(pattern: int, partials, residual: torch.Tensor | None =
                                           float(eps), _ptr(scale_factor), int(T), int(H),
                                           ctypes.byref(outs), TS_FLAG_PDL if launch_with_pdl else 0,
                                           _stream(stream)))
+
+
+def rs_token_split(T: int, world: int, rank: int) -> tuple[int, int]:
+    """(start, count) of rank ``rank``'s token slice: T//world tokens each, the
+    first T % world ranks one more (tokenspeed triton.py `rsag_get_token_dist`)."""
+    base, extra = divmod(T, world)
+    return rank * base + min(rank, extra), base + (1 if rank < extra else 0)
+
+
+def ts_reducescatter_fused_norm(rs_pattern: int, partials, rank: int, add_in: torch.Tensor | None = None,
+                                residual: torch.Tensor | None = None, gamma: torch.Tensor | None = None,
+                                eps: float = 1e-6, scale_factor: torch.Tensor | float | None = None, *,
+                                reducescatter_out: torch.Tensor | None = None,
+                                residual_out: torch.Tensor | None = None,
+                                norm_out: torch.Tensor | None = None,
+                                quant_out: torch.Tensor | None = None,
+                                scale_out: torch.Tensor | None = None,
+                                sf_layout: int = SFLayout.LINEAR, launch_with_pdl: bool = False,
+                                stream=None) -> None:
+    """Rank ``rank``'s reduce-scatter fusion output (see include/ts_fused_norm.h).
+
+    ``partials``: R CUDA bf16 tensors [T, H] holding every token; ``add_in``,
+    ``residual`` and the outputs have the rank's ``count`` rows
+    (``rs_token_split(T, R, rank)``).
+    """
+    parts = [_dev(p, "partials[%d]" % i, torch.bfloat16) for i, p in enumerate(_rows(partials, "partials"))]
+    T, H = parts[0].shape
+    for p in parts:
+        if p.shape != (T, H) or not p.is_contiguous():
+            raise ValueError("every partial must be a contiguous [T, H] tensor")
+    for name, t in (("add_in", add_in), ("residual", residual), ("gamma", gamma),
+                    ("reducescatter_out", reducescatter_out), ("residual_out", residual_out),
+                    ("norm_out", norm_out), ("quant_out", quant_out), ("scale_out", scale_out)):
+        if t is not None:
+            _dev(t, name)
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+    if scale_factor is not None and not isinstance(scale_factor, torch.Tensor):
+        scale_factor = torch.tensor([float(scale_factor)], dtype=torch.float32, device=parts[0].device)
+    if scale_factor is not None:
+        _dev(scale_factor, "scale_factor", torch.float32)
+    outs = TsOuts(_ptr(reducescatter_out), _ptr(residual_out), _ptr(norm_out), None, 0, _ptr(quant_out),
+                  _ptr(scale_out), int(sf_layout), 0)
+    arr = (ctypes.c_void_p * len(parts))(*[p.data_ptr() for p in parts])
+    _check(library().ts_reducescatter_fused_norm(int(rs_pattern), arr, len(parts), int(rank), _ptr(add_in),
+                                                 _ptr(residual), _ptr(gamma), float(eps), _ptr(scale_factor),
+                                                 int(T), int(H), ctypes.byref(outs),
+                                                 TS_FLAG_PDL if launch_with_pdl else 0, _stream(stream)))
+
+
+def ts_allgather_fused_norm(ag_pattern: int, inputs, q_lora_rank: int, kv_lora_rank: int,
+                            qk_rope_head_dim: int, x_gamma: torch.Tensor | None = None,
+                            y_gamma: torch.Tensor | None = None, x_eps: float = 1e-6, y_eps: float = 1e-6, *,
+                            allgather_out: torch.Tensor, x_norm_out: torch.Tensor | None = None,
+                            y_norm_out: torch.Tensor | None = None, quant_out: torch.Tensor | None = None,
+                            scale_out: torch.Tensor | None = None, launch_with_pdl: bool = False,
+                            stream=None) -> None:
+    """All-gather fusion with the dual MLA RMSNorm (see include/ts_fused_norm.h).
+
+    ``inputs``: R CUDA bf16 tensors, rank r's token slice [count_r, hidden]
+    with the counts of ``rs_token_split(T, R, r)``; the outputs have T rows.
+    """
+    ins = [_dev(x, "inputs[%d]" % i, torch.bfloat16) for i, x in enumerate(inputs)]
+    R = len(ins)
+    hidden = q_lora_rank + kv_lora_rank + qk_rope_head_dim
+    T = sum(int(x.shape[0]) for x in ins)
+    for r, x in enumerate(ins):
+        if x.dim() != 2 or x.shape != (rs_token_split(T, R, r)[1], hidden) or not x.is_contiguous():
+            raise ValueError("inputs[r] must be a contiguous [count_r, hidden] slice (rs_token_split counts)")
+    for name, t in (("x_gamma", x_gamma), ("y_gamma", y_gamma), ("allgather_out", allgather_out),
+                    ("x_norm_out", x_norm_out), ("y_norm_out", y_norm_out), ("quant_out", quant_out),
+                    ("scale_out", scale_out)):
+        if t is not None:
+            _dev(t, name)
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+    arr = (ctypes.c_void_p * R)(*[x.data_ptr() for x in ins])
+    _check(library().ts_allgather_fused_norm(int(ag_pattern), arr, R, T, hidden, q_lora_rank, kv_lora_rank,
+                                             qk_rope_head_dim, _ptr(x_gamma), _ptr(y_gamma), float(x_eps),
+                                             float(y_eps), _ptr(allgather_out), _ptr(x_norm_out),
+                                             _ptr(y_norm_out), _ptr(quant_out), _ptr(scale_out),
+                                             TS_FLAG_PDL if launch_with_pdl else 0, _stream(stream)))
 
 
 def ts_qk_norm_sharded(shards, q_shard: int, k_shard: int, q_weight: torch.Tensor,

@@ -1,0 +1,166 @@
+// All-gather fusion with the dual RMSNorm of MLA segments, restated for one
+// GPU (tokenspeed trtllm.py `trtllm_allgather_fusion`, `AllGatherFusionPattern`):
+// the R ranks' token slices (tokenspeed triton.py `rsag_get_token_dist`: T/R
+// tokens each, the first T%R ranks one more) are gathered in rank order, and
+// each gathered row x (q_lora_rank) | y (kv_lora_rank) | rope gets
+//   x_norm = bf16((x * rsqrt(mean(x^2) + x_eps)) * x_gamma)
+//   y_norm = bf16((y * rsqrt(mean(y^2) + y_eps)) * y_gamma)
+// and, for kAllGatherfusedRMSFP8BlockWiseQuant, the x norm in FP8 1x128
+// blocks (s = amax/448, code = e4m3(n / s), 0 for an all-zero block).
+//
+// One warp per gathered row (rows are at most 2112 wide: 264 chunks of 8, at
+// most 9 per lane), 8 rows per CTA.  The row stays in registers as packed
+// bf16; q_lora_rank % 128 == 0 puts the x/y boundary on a half-warp boundary,
+// so the 16-lane shuffles of an FP8 block never mix x with y.
+#include "device_util.cuh"
+#include "launch.h"
+
+namespace tsfn {
+
+namespace {
+
+constexpr int kRowsPerCta = 8;
+
+// At least four 256-thread CTAs (32 warps) per SM: at most 64 registers.
+template <int CPL, int PATTERN>
+__global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_norm_kernel(const __grid_constant__ AGArgs a)
+{
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kRowsPerCta + warp;
+    pdl_wait();
+    if (t >= a.T)
+        return;
+
+    // which rank's slice holds gathered row t
+    const int64_t base = a.T / a.R, extra = a.T % a.R;
+    int rank;
+    int64_t local;
+    if (t < extra * (base + 1)) {
+        rank = (int)(t / (base + 1));
+        local = t - rank * (base + 1);
+    } else {
+        const int64_t t2 = t - extra * (base + 1);
+        rank = (int)(extra + t2 / base);
+        local = t2 - (rank - extra) * base;
+    }
+    const int hidden = a.hidden;
+    const uint16_t *row = a.inputs[rank] + local * hidden;
+    const int nch = hidden >> 3, qc = a.q >> 3, kc = a.kv >> 3;
+
+    uint4 v[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const int c = lane + 32 * i;
+        if (c < nch)
+            v[i] = ld_stream(row + (int64_t)c * 8);
+    }
+    pdl_launch_dependents();
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const int c = lane + 32 * i;
+        if (c < nch)
+            st_v4(a.allgather_out + t * hidden + (int64_t)c * 8, v[i]);
+    }
+    if constexpr (PATTERN == 0)
+        return;
+
+    float sx = 0.0f, sy = 0.0f;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const int c = lane + 32 * i;
+        if (c < qc + kc) {
+            float f[8];
+            unpack8(v[i], f);
+            float s = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                s = fmaf(f[e], f[e], s);
+            if (c < qc)
+                sx += s;
+            else
+                sy += s;
+        }
+    }
+    sx = warp_sum(sx);
+    sy = warp_sum(sy);
+    const float scx = rsqrtf(__fadd_rn(__fdiv_rn(sx, (float)a.q), a.x_eps));
+    const float scy = rsqrtf(__fadd_rn(__fdiv_rn(sy, (float)a.kv), a.y_eps));
+
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const int c = lane + 32 * i;
+        const bool is_x = c < qc;
+        const bool is_y = !is_x && c < qc + kc;
+        float nf[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            nf[e] = 0.0f;
+        if (is_x || is_y) {
+            float f[8], g[8];
+            unpack8(v[i], f);
+            const uint16_t *gam = is_x ? a.x_gamma + (int64_t)c * 8 : a.y_gamma + (int64_t)(c - qc) * 8;
+            unpack8(ld_keep(gam), g);
+            const float sc = is_x ? scx : scy;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                nf[e] = __fmul_rn(__fmul_rn(f[e], sc), g[e]);
+            const uint4 nb = pack8(nf);
+            unpack8(nb, nf);  // the quantiser reads the bf16-rounded norm
+            if (is_x) {
+                if (a.x_norm_out != nullptr)
+                    st_v4(a.x_norm_out + t * a.q + (int64_t)c * 8, nb);
+            } else {
+                st_v4(a.y_norm_out + t * a.kv + (int64_t)(c - qc) * 8, nb);
+            }
+        }
+        if constexpr (PATTERN == 2) {
+            // 16 lanes = one 128-column block of x; every lane takes part
+            float amax = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                amax = fmaxf(amax, fabsf(nf[e]));
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            if (is_x) {
+                const float sg = __fdiv_rn(amax, 448.0f);
+                if ((c & 15) == 0)
+                    st_f32(a.scale_out + t * (a.q >> 7) + (c >> 4), sg);
+                uint2 codes = make_uint2(0, 0);
+                if (sg != 0.0f) {
+                    float q[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        q[e] = __fdiv_rn(nf[e], sg);
+                    codes = cvt_e4m3x8(q);
+                }
+                st_v2(a.quant_out + t * a.q + (int64_t)c * 8, codes);
+            }
+        }
+    }
+}
+
+template <int CPL>
+cudaError_t launch_cpl(const AGArgs &a, bool pdl, cudaStream_t s)
+{
+    const dim3 g((unsigned)((a.T + kRowsPerCta - 1) / kRowsPerCta)), b(kRowsPerCta * 32);
+    switch (a.pattern) {
+    case 0: return launch_kernel(ag_norm_kernel<CPL, 0>, g, b, 0, s, pdl, a);
+    case 1: return launch_kernel(ag_norm_kernel<CPL, 1>, g, b, 0, s, pdl, a);
+    default: return launch_kernel(ag_norm_kernel<CPL, 2>, g, b, 0, s, pdl, a);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_ag(const AGArgs &a, bool pdl, cudaStream_t stream)
+{
+    const int per_lane = (a.hidden / 8 + 31) / 32;  // 1..9
+    if (per_lane <= 1) return launch_cpl<1>(a, pdl, stream);
+    if (per_lane <= 2) return launch_cpl<2>(a, pdl, stream);
+    if (per_lane <= 4) return launch_cpl<4>(a, pdl, stream);
+    return launch_cpl<9>(a, pdl, stream);
+}
+
+}  // namespace tsfn

@@ -94,13 +94,15 @@ extern "C" const char *ts_status_string(int status)
 
 extern "C" const char *ts_last_error_detail(void) { return g_detail; }
 
-extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, int R,
-                                    const void *residual, const void *gamma, float eps,
-                                    const float *scale_factor, int64_t T, int64_t H,
-                                    const ts_outs_t *outs, uint32_t flags, void *stream)
+namespace {
+
+// Checks and launch of one all-reduce-form pattern (0..8) over T rows.  The
+// reduce-scatter entry point lands here too, with the partial pointers
+// already moved to the rank's token slice and add_in set for its "Add" codes.
+int fused_impl(int pattern, const void *const *partials, int R, const void *add_in, bool needs_add,
+               const void *residual, const void *gamma, float eps, const float *scale_factor,
+               int64_t T, int64_t H, const ts_outs_t *outs, uint32_t flags, void *stream)
 {
-    if (pattern < 0 || pattern > 8)
-        return fail(TS_ERR_BAD_PATTERN, "pattern %d is not an AllReduceFusionPattern code (0..8)", pattern);
     if (outs == nullptr)
         return fail(TS_ERR_NULL, "outs is NULL");
     if (partials == nullptr)
@@ -140,6 +142,14 @@ extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, in
             return fail(TS_ERR_ALIGN, "residual is not 16-byte aligned");
         if (!aligned(gamma, 16))
             return fail(TS_ERR_ALIGN, "gamma is not 16-byte aligned");
+    }
+    if (needs_add) {
+        if (add_in == nullptr && !empty)
+            return fail(TS_ERR_NULL, "add_in is NULL (required for the reduce-scatter Add patterns)");
+        if (!aligned(add_in, 16))
+            return fail(TS_ERR_ALIGN, "add_in is not 16-byte aligned");
+    } else if (add_in != nullptr) {
+        return fail(TS_ERR_UNSUPPORTED, "add_in is only an input of the reduce-scatter Add patterns (7, 8)");
     }
     const bool needs_scale = pattern >= 2 && pattern <= 5;
     if (needs_scale) {
@@ -213,6 +223,8 @@ extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, in
             if (overlap(outs_s[i], span(gamma, H * 2, "")))
                 return fail(TS_ERR_ALIAS, "%s overlaps gamma", kOutputNames[i]);
         }
+        if (needs_add && overlap(outs_s[i], span(add_in, elems * 2, "")))
+            return fail(TS_ERR_ALIAS, "%s overlaps add_in", kOutputNames[i]);
         if (needs_scale && overlap(outs_s[i], span(scale_factor, 4, "")))
             return fail(TS_ERR_ALIAS, "%s overlaps scale_factor", kOutputNames[i]);
     }
@@ -224,6 +236,7 @@ extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, in
     for (int r = 0; r < R; ++r)
         a.partials[r] = static_cast<const uint16_t *>(partials[r]);
     a.R = R;
+    a.add_in = needs_add ? static_cast<const uint16_t *>(add_in) : nullptr;
     a.residual = static_cast<const uint16_t *>(residual);
     a.gamma = static_cast<const uint16_t *>(gamma);
     a.eps = eps;
@@ -258,6 +271,53 @@ extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, in
         return fail(TS_ERR_LAUNCH, "kernel launch failed: %s (%s)", cudaGetErrorName(err),
                     cudaGetErrorString(err));
     return ok();
+}
+
+}  // namespace
+
+extern "C" int ts_fused_reduce_norm(int pattern, const void *const *partials, int R,
+                                    const void *residual, const void *gamma, float eps,
+                                    const float *scale_factor, int64_t T, int64_t H,
+                                    const ts_outs_t *outs, uint32_t flags, void *stream)
+{
+    if (pattern < 0 || pattern > 8)
+        return fail(TS_ERR_BAD_PATTERN, "pattern %d is not an AllReduceFusionPattern code (0..8)", pattern);
+    return fused_impl(pattern, partials, R, nullptr, false, residual, gamma, eps, scale_factor, T, H, outs,
+                      flags, stream);
+}
+
+extern "C" int ts_reducescatter_fused_norm(int rs_pattern, const void *const *partials, int R, int rank,
+                                           const void *add_in, const void *residual, const void *gamma,
+                                           float eps, const float *scale_factor, int64_t T, int64_t H,
+                                           const ts_outs_t *outs, uint32_t flags, void *stream)
+{
+    if (rs_pattern < 0 || rs_pattern > 8)
+        return fail(TS_ERR_BAD_PATTERN, "rs_pattern %d is not a ReduceScatterFusionPattern code (0..8)",
+                    rs_pattern);
+    if (partials == nullptr)
+        return fail(TS_ERR_NULL, "partials is NULL");
+    if (R < 1 || R > tsfn::kMaxR)
+        return fail(TS_ERR_SHAPE, "R = %d outside 1..%d", R, tsfn::kMaxR);
+    if (rank < 0 || rank >= R)
+        return fail(TS_ERR_SHAPE, "rank = %d outside 0..R-1 (R = %d)", rank, R);
+    if (T < 0 || T > kMaxRows)
+        return fail(TS_ERR_SHAPE, "T = %lld outside 0..%lld", (long long)T, (long long)kMaxRows);
+    if (H < 8 || H % 8 != 0)
+        return fail(TS_ERR_SHAPE, "H = %lld must be a positive multiple of 8", (long long)H);
+    // token slice of `rank` (T/R each, the first T%R ranks one more)
+    const int64_t base = T / R, extra = T % R;
+    const int64_t count = base + (rank < extra ? 1 : 0);
+    const int64_t start = rank * base + (rank < extra ? rank : extra);
+    const void *sliced[tsfn::kMaxR];
+    for (int r = 0; r < R; ++r) {
+        if (partials[r] == nullptr && T > 0)
+            return fail(TS_ERR_NULL, "partials[%d] is NULL", r);
+        sliced[r] = partials[r] == nullptr ? nullptr
+                                           : static_cast<const uint16_t *>(partials[r]) + start * H;
+    }
+    const int form = rs_pattern == 7 ? 6 : (rs_pattern == 8 ? 1 : rs_pattern);
+    return fused_impl(form, sliced, R, add_in, rs_pattern >= 7, residual, gamma, eps, scale_factor, count, H,
+                      outs, flags, stream);
 }
 
 namespace {
@@ -369,4 +429,101 @@ extern "C" int ts_rms_norm_sharded(const void *const *shards, int R, int64_t T, 
 {
     return sharded_norm("shards", shards, R, T, row_stride, width, 0, weight, nullptr, eps, out, ldo,
                         nullptr, 0, flags, stream);
+}
+
+extern "C" int ts_allgather_fused_norm(int ag_pattern, const void *const *inputs, int R, int64_t T,
+                                       int64_t hidden, int64_t q_lora_rank, int64_t kv_lora_rank,
+                                       int64_t qk_rope_head_dim, const void *x_gamma, const void *y_gamma,
+                                       float x_eps, float y_eps, void *allgather_out, void *x_norm_out,
+                                       void *y_norm_out, void *quant_out, void *scale_out, uint32_t flags,
+                                       void *stream)
+{
+    if (ag_pattern < 0 || ag_pattern > 2)
+        return fail(TS_ERR_BAD_PATTERN, "ag_pattern %d is not an AllGatherFusionPattern code (0..2)", ag_pattern);
+    if (inputs == nullptr)
+        return fail(TS_ERR_NULL, "inputs is NULL");
+    if (R < 1 || R > tsfn::kMaxR)
+        return fail(TS_ERR_SHAPE, "R = %d outside 1..%d", R, tsfn::kMaxR);
+    if (T < 0 || T > kMaxRows)
+        return fail(TS_ERR_SHAPE, "T = %lld outside 0..%lld", (long long)T, (long long)kMaxRows);
+    if (flags & ~kKnownFlags)
+        return fail(TS_ERR_UNSUPPORTED, "unknown flag bits 0x%x", flags & ~kKnownFlags);
+    const int64_t q = q_lora_rank, kv = kv_lora_rank, rope = qk_rope_head_dim;
+    if (q <= 0 || q % 128 != 0)
+        return fail(TS_ERR_SHAPE, "q_lora_rank = %lld must be a positive multiple of 128", (long long)q);
+    if (kv <= 0 || kv % 8 != 0 || rope < 0 || rope % 8 != 0)
+        return fail(TS_ERR_SHAPE, "kv_lora_rank (%lld) and qk_rope_head_dim (%lld) must be multiples of 8",
+                    (long long)kv, (long long)rope);
+    if (q + kv + rope != hidden)
+        return fail(TS_ERR_SHAPE, "q_lora_rank + kv_lora_rank + qk_rope_head_dim (%lld) != hidden (%lld)",
+                    (long long)(q + kv + rope), (long long)hidden);
+    if (hidden > 2112)
+        return fail(TS_ERR_SHAPE, "hidden = %lld above 2112", (long long)hidden);
+    const bool empty = T == 0;
+    const int64_t base = T / R, extra = T % R;
+    for (int r = 0; r < R; ++r) {
+        const int64_t count = base + (r < extra ? 1 : 0);
+        if (inputs[r] == nullptr && count > 0)
+            return fail(TS_ERR_NULL, "inputs[%d] is NULL", r);
+        if (!aligned(inputs[r], 16))
+            return fail(TS_ERR_ALIGN, "inputs[%d] is not 16-byte aligned", r);
+    }
+    if (ag_pattern != 0) {
+        if (x_gamma == nullptr || y_gamma == nullptr)
+            return fail(TS_ERR_NULL, "x_gamma and y_gamma are required for pattern %d", ag_pattern);
+        if (!aligned(x_gamma, 16) || !aligned(y_gamma, 16))
+            return fail(TS_ERR_ALIGN, "x_gamma / y_gamma are not 16-byte aligned");
+    }
+    // outputs: allgather_out always; x_norm_out 1 (optional in 2); y_norm_out 1, 2; quant/scale 2
+    void *const outp[5] = {allgather_out, x_norm_out, y_norm_out, quant_out, scale_out};
+    const char *const names[5] = {"allgather_out", "x_norm_out", "y_norm_out", "quant_out", "scale_out"};
+    const char *const table[3] = {"R----", "RRR--", "RoRRR"};
+    for (int i = 0; i < 5; ++i) {
+        const char need = table[ag_pattern][i];
+        if (need == 'R' && outp[i] == nullptr && !empty)
+            return fail(TS_ERR_NULL, "%s is required for pattern %d", names[i], ag_pattern);
+        if (need == '-' && outp[i] != nullptr)
+            return fail(TS_ERR_UNSUPPORTED, "%s is not an output of pattern %d (pass NULL)", names[i], ag_pattern);
+        if (outp[i] != nullptr && !aligned(outp[i], i == 4 ? 4 : 16))
+            return fail(TS_ERR_ALIGN, "%s is not %d-byte aligned", names[i], i == 4 ? 4 : 16);
+    }
+    if (empty)
+        return ok();
+    const int64_t out_bytes[5] = {T * hidden * 2, T * q * 2, T * kv * 2, T * q, T * (q / 128) * 4};
+    Span os[5];
+    for (int i = 0; i < 5; ++i)
+        os[i] = span(outp[i], outp[i] ? out_bytes[i] : 0, names[i]);
+    for (int i = 0; i < 5; ++i) {
+        for (int j = i + 1; j < 5; ++j)
+            if (overlap(os[i], os[j]))
+                return fail(TS_ERR_ALIAS, "%s overlaps %s", os[i].name, os[j].name);
+        for (int r = 0; r < R; ++r)
+            if (overlap(os[i], span(inputs[r], (base + (r < extra ? 1 : 0)) * hidden * 2, "")))
+                return fail(TS_ERR_ALIAS, "%s overlaps inputs[%d]", os[i].name, r);
+        if (ag_pattern != 0 && (overlap(os[i], span(x_gamma, q * 2, "")) || overlap(os[i], span(y_gamma, kv * 2, ""))))
+            return fail(TS_ERR_ALIAS, "%s overlaps a gamma", os[i].name);
+    }
+
+    tsfn::AGArgs a{};
+    for (int r = 0; r < R; ++r)
+        a.inputs[r] = static_cast<const uint16_t *>(inputs[r]);
+    a.R = R;
+    a.T = T;
+    a.hidden = (int)hidden;
+    a.q = (int)q;
+    a.kv = (int)kv;
+    a.x_gamma = static_cast<const uint16_t *>(x_gamma);
+    a.y_gamma = static_cast<const uint16_t *>(y_gamma);
+    a.x_eps = x_eps;
+    a.y_eps = y_eps;
+    a.pattern = ag_pattern;
+    a.allgather_out = static_cast<uint16_t *>(allgather_out);
+    a.x_norm_out = static_cast<uint16_t *>(x_norm_out);
+    a.y_norm_out = static_cast<uint16_t *>(y_norm_out);
+    a.quant_out = static_cast<uint8_t *>(quant_out);
+    a.scale_out = static_cast<float *>(scale_out);
+    const cudaError_t err = tsfn::launch_ag(a, (flags & TS_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess)
+        return fail(TS_ERR_LAUNCH, "kernel launch failed: %s (%s)", cudaGetErrorName(err), cudaGetErrorString(err));
+    return ok();
 }

@@ -4,7 +4,8 @@
 // The math is the one of tokenspeed triton.py `amd_allreduce_residual_rmsnorm_kernel`
 // (and `amd_all_reduce_kernel` for kAllReduce): the R partials are widened to
 // fp32 and added in ascending order into an accumulator that starts at +0,
-// the residual is added in fp32, the row's mean of squares of that unrounded
+// the optional add_in of the reduce-scatter "Add" patterns (trtllm.py
+// `ReduceScatterFusionPattern`) and then the residual are added in fp32, the row's mean of squares of that unrounded
 // fp32 x gives s = rsqrt(mean + eps), and n = bf16((x * s) * gamma).  The
 // quantisers of trtllm.py `AllReduceFusionPattern` then read n:
 //   FP8 per tensor   code = e4m3(n * sigma)
@@ -27,8 +28,21 @@ namespace {
 
 constexpr int kMaxThreads = 512;
 
-template <int RB, int V, Epilogue EP>
-__global__ void __launch_bounds__(kMaxThreads) fused_rows_kernel(const __grid_constant__ FusedArgs a)
+// Register cap per instance (CTAs have at most kMaxThreads = 512 threads, so
+// every cap <= 128 keeps a full CTA launchable): at most 8 partials and 2
+// chunks per thread must leave room for two 512-thread CTAs per SM (64
+// registers), and with at most 4 partials (no add_in) for four 320-thread
+// CTAs (48; registers are allocated in steps of 8 per thread).  The tests check that no
+// instance spills.
+template <int RB, int V, bool ADD>
+constexpr int reg_cap()
+{
+    return (RB <= 4 && V <= 2 && !ADD) ? 48 : ((RB <= 8 && V <= 2) ? 64 : 128);
+}
+
+template <int RB, int V, Epilogue EP, bool ADD>
+__global__ void __maxnreg__((reg_cap<RB, V, ADD>()))
+    fused_rows_kernel(const __grid_constant__ FusedArgs a)
 {
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
@@ -61,9 +75,12 @@ __global__ void __launch_bounds__(kMaxThreads) fused_rows_kernel(const __grid_co
             for (int r = 0; r < RB; ++r)
                 if (r < a.R)
                     raw[r] = ld_stream(a.partials[r] + off);
-            uint4 res;
-            if constexpr (EP != Epilogue::kAllReduce)
+            uint4 res, addv;
+            if constexpr (EP != Epilogue::kAllReduce) {
                 res = ld_stream(a.residual + off);
+                if constexpr (ADD)
+                    addv = ld_stream(a.add_in + off);
+            }
             float acc[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -82,6 +99,12 @@ __global__ void __launch_bounds__(kMaxThreads) fused_rows_kernel(const __grid_co
                 st_v4(a.allreduce_out + off, pack8(acc));
             if constexpr (EP != Epilogue::kAllReduce) {
                 float f[8];
+                if constexpr (ADD) {  // x = ((sum) + add_in) + residual
+                    unpack8(addv, f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        acc[e] = __fadd_rn(acc[e], f[e]);
+                }
                 unpack8(res, f);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -114,6 +137,12 @@ __global__ void __launch_bounds__(kMaxThreads) fused_rows_kernel(const __grid_co
     float qscale = 0.0f;
     if constexpr (EP == Epilogue::kFp8Tensor || EP == Epilogue::kFp4)
         qscale = __ldg(a.scale_factor);
+    uint8_t *sf_row = nullptr;  // this row's scale factors (NVFP4)
+    int sf_stride = 0;
+    if constexpr (EP == Epilogue::kFp4) {
+        sf_row = static_cast<uint8_t *>(a.scale_out) + sf_row_base(a, row);
+        sf_stride = sf_tile_stride(a);
+    }
 
     // ---- phase 2: norm and the pattern's outputs ----------------------------
 #pragma unroll
@@ -197,14 +226,14 @@ __global__ void __launch_bounds__(kMaxThreads) fused_rows_kernel(const __grid_co
             const uint32_t s2 = __shfl_down_sync(0xffffffffu, sf, 2);
             const uint32_t s4 = __shfl_down_sync(0xffffffffu, sf, 4);
             const uint32_t s6 = __shfl_down_sync(0xffffffffu, sf, 6);
-            uint8_t *sfp = static_cast<uint8_t *>(a.scale_out);
-            const int64_t k = c >> 1;
+            const int k = c >> 1;
+            uint8_t *sfk = sf_row + (k >> 2) * sf_stride + (k & 3);
             if (live) {
                 if ((a.H & 63) == 0) {
                     if ((lane & 7) == 0)
-                        st_u32(sfp + sf_offset(a, row, k), sf | (s2 << 8) | (s4 << 16) | (s6 << 24));
+                        st_u32(sfk, sf | (s2 << 8) | (s4 << 16) | (s6 << 24));
                 } else if ((c & 1) == 0) {
-                    st_u8(sfp + sf_offset(a, row, k), sf);
+                    st_u8(sfk, sf);
                 }
             }
         }
@@ -212,11 +241,9 @@ __global__ void __launch_bounds__(kMaxThreads) fused_rows_kernel(const __grid_co
 
     if constexpr (EP == Epilogue::kFp4) {
         // zero the padding columns of this row in the swizzled layout
-        if (a.sf_layout != kSfLinear && tid == 0) {
-            uint8_t *sfp = static_cast<uint8_t *>(a.scale_out);
-            for (int64_t k = a.H >> 4; k < a.sf_cols; ++k)
-                st_u8(sfp + sf_offset(a, row, k), 0u);
-        }
+        if (a.sf_layout != kSfLinear && tid == 0)
+            for (int k = (int)(a.H >> 4); k < a.sf_cols; ++k)
+                st_u8(sf_row + (k >> 2) * sf_stride + (k & 3), 0u);
     }
 }
 
@@ -224,12 +251,22 @@ template <int RB, int V>
 cudaError_t launch_rb_v(Epilogue ep, const FusedArgs &a, int nthr, int64_t grid, bool pdl, cudaStream_t s)
 {
     const dim3 g((unsigned)grid), b((unsigned)nthr);
+    const bool add = a.add_in != nullptr;  // only with kNorm / kFp8Block (the reduce-scatter Add codes)
     switch (ep) {
-    case Epilogue::kAllReduce: return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kAllReduce>, g, b, 0, s, pdl, a);
-    case Epilogue::kNorm: return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm>, g, b, 0, s, pdl, a);
-    case Epilogue::kFp8Tensor: return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Tensor>, g, b, 0, s, pdl, a);
-    case Epilogue::kFp4: return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp4>, g, b, 0, s, pdl, a);
-    case Epilogue::kFp8Block: return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block>, g, b, 0, s, pdl, a);
+    case Epilogue::kAllReduce:
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kAllReduce, false>, g, b, 0, s, pdl, a);
+    case Epilogue::kNorm:
+        if (add)
+            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, true>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, false>, g, b, 0, s, pdl, a);
+    case Epilogue::kFp8Tensor:
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Tensor, false>, g, b, 0, s, pdl, a);
+    case Epilogue::kFp4:
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp4, false>, g, b, 0, s, pdl, a);
+    case Epilogue::kFp8Block:
+        if (add)
+            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, true>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, false>, g, b, 0, s, pdl, a);
     }
     return cudaErrorInvalidValue;
 }

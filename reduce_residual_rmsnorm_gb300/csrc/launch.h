@@ -28,6 +28,7 @@ enum class Epilogue : int {
 struct FusedArgs {
     const uint16_t *partials[kMaxR];
     int R;
+    const uint16_t *add_in;  // optional extra addend before the residual (reduce-scatter "Add")
     const uint16_t *residual;
     const uint16_t *gamma;
     float eps;
@@ -62,6 +63,22 @@ struct QKArgs {
     int64_t ldk;
 };
 
+struct AGArgs {
+    const uint16_t *inputs[kMaxR];  // rank r's token slice [count_r, hidden]
+    int R;
+    int64_t T;                      // gathered tokens
+    int hidden, q, kv;              // row = x (q) | y (kv) | rope
+    const uint16_t *x_gamma;
+    const uint16_t *y_gamma;
+    float x_eps, y_eps;
+    int pattern;                    // AllGatherFusionPattern 0..2
+    uint16_t *allgather_out;        // [T, hidden]
+    uint16_t *x_norm_out;           // [T, q] (optional in pattern 2)
+    uint16_t *y_norm_out;           // [T, kv]
+    uint8_t *quant_out;             // [T, q] e4m3 (pattern 2)
+    float *scale_out;               // [T, q/128] (pattern 2)
+};
+
 // Launch `kernel` on `stream`, with programmatic stream serialisation when
 // `pdl` is set (the kernel then overlaps its launch with the previous
 // kernel's tail and waits for it in pdl_wait()).
@@ -83,6 +100,7 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 }
 
 cudaError_t launch_fused(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t stream);
+cudaError_t launch_ag(const AGArgs &a, bool pdl, cudaStream_t stream);
 // Sharded RMSNorm over one (K == 0) or two (q and k) segments of each shard row.
 cudaError_t launch_qk(const QKArgs &a, bool pdl, cudaStream_t stream);
 

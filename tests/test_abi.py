@@ -293,3 +293,111 @@ def test_pdl_flag_accepted(lib):
     assert _fused_call(lib, T=0, flags=1)[0] == TS_OK
     assert _qk_call(lib, T=0, flags=1)[0] == TS_OK
     assert _rms_call(lib, T=0, flags=1)[0] == TS_OK
+
+
+# ---------------------------------------------------------------------------
+# ts_reducescatter_fused_norm
+# ---------------------------------------------------------------------------
+
+def _rs_call(lib, rs=8, R=4, rank=0, T=16, H=256, add=True, flags=0, mutate=None):
+    f = Fake()
+    parts = [f() for _ in range(R)]
+    a = dict(rs=rs, partials=parts, R=R, rank=rank, add_in=f() if add else None, residual=f(), gamma=f(),
+             sf=f(), T=T, H=H, flags=flags)
+    form = {7: 6, 8: 1}.get(rs, rs)
+    table = {0: "R-----", 1: "oRR---", 2: "oR--R-", 3: "oR--RR", 4: "oRR-R-", 5: "oRR-RR", 6: "oR--RR"}
+    row = table.get(form, "oRR---")
+    keys = ["allreduce_out", "residual_out", "norm_out", "partial_norm_out", "quant_out", "scale_out"]
+    outs = {k: (f() if row[i] == "R" else None) for i, k in enumerate(keys)}
+    if mutate:
+        mutate(a, outs)
+    o = TsOuts(outs["allreduce_out"], outs["residual_out"], outs["norm_out"], outs["partial_norm_out"], 0,
+               outs["quant_out"], outs["scale_out"], 2, 0)
+    arr = None if a["partials"] is None else (ctypes.c_void_p * len(a["partials"]))(*a["partials"])
+    st = lib.ts_reducescatter_fused_norm(a["rs"], arr, a["R"], a["rank"], a["add_in"], a["residual"], a["gamma"],
+                                         1e-6, a["sf"], a["T"], a["H"], ctypes.byref(o), a["flags"], None)
+    return st, lib.ts_last_error_detail().decode()
+
+
+def test_rs_valid_empty_calls(lib):
+    assert _rs_call(lib, T=0)[0] == TS_OK
+    assert _rs_call(lib, T=2, R=4, rank=3)[0] == TS_OK  # rank 3 of 4 owns no token of 2
+
+
+NEG_RS = [
+    ("rs pattern 9", dict(rs=9), BAD_PATTERN),
+    ("rank -1", dict(rank=-1), SHAPE),
+    ("rank == R", dict(rank=4), SHAPE),
+    ("add_in missing for 8", dict(add=False), NULL),
+    ("add_in missing for 7", dict(rs=7, add=False), NULL),
+    ("add_in given for 1", dict(rs=1, add=True), UNSUPPORTED),
+    ("add_in misaligned", dict(mutate=lambda a, o: a.update(add_in=a["add_in"] + 4)), ALIGN),
+    ("partial out given", dict(mutate=lambda a, o: o.update(partial_norm_out=0x10000)), UNSUPPORTED),
+    ("output overlaps add_in", dict(mutate=lambda a, o: o.update(norm_out=a["add_in"])), ALIAS),
+    ("H % 8", dict(H=100), SHAPE),
+    ("partials NULL", dict(mutate=lambda a, o: a.update(partials=None)), NULL),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", NEG_RS, ids=[c[0] for c in NEG_RS])
+def test_rs_rejects(lib, name, kw, want):
+    st, detail = _rs_call(lib, **kw)
+    assert st == want, (name, st, detail)
+    assert detail
+
+
+# ---------------------------------------------------------------------------
+# ts_allgather_fused_norm
+# ---------------------------------------------------------------------------
+
+def _ag_call(lib, pat=1, R=8, T=64, q=1536, kv=512, rope=64, hidden=None, flags=0, mutate=None):
+    f = Fake()
+    a = dict(pat=pat, inputs=[f() for _ in range(R)], R=R, T=T, hidden=q + kv + rope if hidden is None else hidden,
+             q=q, kv=kv, rope=rope, xg=f(), yg=f(), flags=flags)
+    table = {0: "R----", 1: "RRR--", 2: "RoRRR"}
+    keys = ["allgather_out", "x_norm_out", "y_norm_out", "quant_out", "scale_out"]
+    outs = {k: (f() if table.get(pat, "RRR--")[i] == "R" else None) for i, k in enumerate(keys)}
+    if mutate:
+        mutate(a, outs)
+    arr = None if a["inputs"] is None else (ctypes.c_void_p * len(a["inputs"]))(*a["inputs"])
+    st = lib.ts_allgather_fused_norm(a["pat"], arr, a["R"], a["T"], a["hidden"], a["q"], a["kv"], a["rope"],
+                                     a["xg"], a["yg"], 1e-6, 1e-6, *[outs[k] for k in keys], a["flags"], None)
+    return st, lib.ts_last_error_detail().decode()
+
+
+def test_ag_valid_empty_calls(lib):
+    for pat in (0, 1, 2):
+        assert _ag_call(lib, pat=pat, T=0)[0] == TS_OK
+    st, d = _ag_call(lib, pat=1, T=0, mutate=lambda a, o: (a.update(inputs=[None] * 8),
+                                                          o.update(allgather_out=None, x_norm_out=None,
+                                                                   y_norm_out=None)))
+    assert st == TS_OK, d
+
+
+NEG_AG = [
+    ("pattern 3", dict(pat=3), BAD_PATTERN),
+    ("inputs NULL", dict(mutate=lambda a, o: a.update(inputs=None)), NULL),
+    ("R 17", dict(R=17), SHAPE),
+    ("q % 128", dict(q=1544, hidden=1544 + 512 + 64), SHAPE),
+    ("kv % 8", dict(kv=500, hidden=1536 + 500 + 64), SHAPE),
+    ("segments != hidden", dict(hidden=2104), SHAPE),
+    ("hidden > 2112", dict(q=1664, hidden=1664 + 512 + 64), SHAPE),
+    ("an input NULL", dict(mutate=lambda a, o: a["inputs"].__setitem__(2, None)), NULL),
+    ("input misaligned", dict(mutate=lambda a, o: a["inputs"].__setitem__(2, a["inputs"][2] + 8)), ALIGN),
+    ("x_gamma NULL", dict(mutate=lambda a, o: a.update(xg=None)), NULL),
+    ("allgather_out NULL", dict(mutate=lambda a, o: o.update(allgather_out=None)), NULL),
+    ("y_norm_out NULL p2", dict(pat=2, mutate=lambda a, o: o.update(y_norm_out=None)), NULL),
+    ("quant_out given to p1", dict(mutate=lambda a, o: o.update(quant_out=0x10000)), UNSUPPORTED),
+    ("x_norm_out given to p0", dict(pat=0, mutate=lambda a, o: o.update(x_norm_out=0x10000)), UNSUPPORTED),
+    ("scale_out misaligned", dict(pat=2, mutate=lambda a, o: o.update(scale_out=o["scale_out"] + 2)), ALIGN),
+    ("x_norm overlaps y_norm", dict(mutate=lambda a, o: o.update(y_norm_out=o["x_norm_out"] + 64)), ALIAS),
+    ("output overlaps an input", dict(mutate=lambda a, o: o.update(allgather_out=a["inputs"][3])), ALIAS),
+    ("unknown flag", dict(flags=2), UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", NEG_AG, ids=[c[0] for c in NEG_AG])
+def test_ag_rejects(lib, name, kw, want):
+    st, detail = _ag_call(lib, **kw)
+    assert st == want, (name, st, detail)
+    assert detail

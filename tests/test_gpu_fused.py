@@ -352,3 +352,66 @@ def test_pdl_dependent_chain_matches_plain(dev):
     for pattern in (1, 6):
         for x, y in zip(chain(False, pattern), chain(True, pattern)):
             assert np.array_equal(x, y)
+
+
+# ---------------------------------------------------------------------------
+# reduce-scatter fusion restated for one GPU (every rank's slice)
+# ---------------------------------------------------------------------------
+
+RS_SHAPES = [(4, 37, 1024), (8, 64, 7168), (3, 2, 256), (2, 16, 4096)]
+
+
+@pytest.mark.parametrize("R,T,H", RS_SHAPES, ids=[f"R{r}-T{t}-H{h}" for r, t, h in RS_SHAPES])
+@pytest.mark.parametrize("rs", list(range(9)))
+def test_reducescatter_every_rank(dev, rs, R, T, H):
+    form = {7: 6, 8: 1}.get(rs, rs)
+    if not _ok_for(form, H):
+        pytest.skip("H not a multiple of the quantisation group")
+    inp = _inputs(R, T, H, seed=100 + rs + R + T)
+    g = torch.Generator().manual_seed(rs + T)
+    add_full = torch.randn((T, H), generator=g).to(torch.bfloat16)
+    scale = {2: 40.0, 4: 40.0, 3: 300.0, 5: 300.0}.get(form)
+    parts = inp["partials"].to(dev)
+    gamma = inp["gamma"].to(dev)
+    for rank in range(R):
+        start, count = pkg.rs_token_split(T, R, rank)
+        res = inp["residual"][start:start + count]
+        add = add_full[start:start + count] if rs >= 7 else None
+        outs = guarded_outputs(form, count, H, dev, 0, 2, allreduce=True)
+        kw = {("reducescatter_out" if k == "allreduce_out" else k): v.t for k, v in outs.items()}
+        sf = None if scale is None else torch.tensor([scale], dtype=torch.float32, device=dev)
+        pkg.ts_reducescatter_fused_norm(rs, parts, rank, None if add is None else add.to(dev),
+                                        None if form == 0 else res.to(dev), None if form == 0 else gamma,
+                                        EPS, sf, **kw)
+        torch.cuda.synchronize()
+        for k, v in outs.items():
+            assert v.intact(), f"write outside {k}"
+        if count == 0:
+            continue
+        got = {k: host(v.t) for k, v in outs.items()}
+        want = oracle.reducescatter_fused_norm(rs, [wl.bits(p) for p in inp["partials"]], rank,
+                                               None if add is None else wl.bits(add), wl.bits(res),
+                                               wl.bits(inp["gamma"]), EPS, scale or 0.0)
+        want["allreduce_out"] = want.pop("reducescatter_out")
+        _compare(form, got, want, LIN, count)
+
+
+def test_reducescatter_slices_equal_allreduce_rows(dev):
+    """With no add_in, the eight rank slices of kRSResidualRMSNorm are the
+    kARResidualRMSNorm rows, bit for bit (same kernel arithmetic)."""
+    R, T, H = 8, 1000, 7168
+    inp = _inputs(R, T, H, seed=12)
+    full = _run_gpu(dev, 1, inp)
+    parts = inp["partials"].to(dev)
+    for rank in range(R):
+        start, count = pkg.rs_token_split(T, R, rank)
+        ro = torch.empty((count, H), dtype=torch.bfloat16, device=dev)
+        no = torch.empty_like(ro)
+        rso = torch.empty_like(ro)
+        pkg.ts_reducescatter_fused_norm(1, parts, rank, None, inp["residual"][start:start + count].to(dev),
+                                        inp["gamma"].to(dev), EPS, reducescatter_out=rso, residual_out=ro,
+                                        norm_out=no)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(rso), full["allreduce_out"][start:start + count])
+        assert np.array_equal(host(ro), full["residual_out"][start:start + count])
+        assert np.array_equal(host(no), full["norm_out"][start:start + count])

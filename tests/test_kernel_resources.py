@@ -1,0 +1,82 @@
+"""Register and spill budget of the kernels (ptxas -v on a CPU build).
+
+These kernels are HBM-bound and reach the roofline only with enough warps per
+SM to keep every thread's 16-byte loads in flight: the fused row kernel must
+fit two CTAs of up to 512 threads per SM (<= 64 registers) wherever it holds
+at most 8 partials and 2 chunks per thread, which covers every benchmarked
+workload.  No kernel may spill.
+"""
+import os
+import re
+import subprocess
+
+import pytest
+
+from reduce_residual_rmsnorm_gb300 import build as libbuild
+
+
+@pytest.fixture(scope="module")
+def resources(tmp_path_factory):
+    out = tmp_path_factory.mktemp("ptxas")
+    res = {}
+    for src in libbuild.sources():
+        if os.path.basename(src) == "api.cu":
+            continue
+        cmd = [libbuild.nvcc(), *libbuild.ARCH, *libbuild.NVCC_FLAGS, "-Xptxas", "-v", "-c", src, "-o",
+               str(out / (os.path.basename(src) + ".o"))]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+        name = None
+        for line in r.stderr.splitlines():
+            m = re.search(r"Compiling entry function '(\S+)'", line)
+            if m:
+                name = m.group(1)
+                res[name] = {}
+                continue
+            if name is None:
+                continue
+            m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+            if m:
+                res[name]["spill"] = int(m.group(1)) + int(m.group(2))
+            m = re.search(r"Used (\d+) registers", line)
+            if m:
+                res[name]["regs"] = int(m.group(1))
+    return res
+
+
+def test_no_kernel_spills(resources):
+    spilled = {k: v for k, v in resources.items() if v.get("spill", 0)}
+    assert not spilled, spilled
+
+
+def test_fused_row_kernel_register_tiers(resources):
+    """<= 8 partials, <= 2 chunks per thread: two 512-thread CTAs per SM (64);
+    <= 4 partials without add_in: four 320-thread CTAs per SM (48)."""
+    # mangled template arguments: fused_rows_kernel<RB, V, Epilogue, ADD>
+    checked = 0
+    for name, v in resources.items():
+        m = re.search(r"fused_rows_kernelILi(\d+)ELi(\d+)ELNS_8EpilogueE\dELb(\d)", name)
+        if m and int(m.group(1)) <= 8 and int(m.group(2)) <= 2:
+            cap = 48 if int(m.group(1)) <= 4 and m.group(3) == "0" else 64
+            assert v["regs"] <= cap, (name, v)
+            checked += 1
+    assert checked >= 20
+
+
+def test_allgather_norm_kernel_fits_four_ctas_per_sm(resources):
+    checked = 0
+    for name, v in resources.items():
+        if "ag_norm_kernel" in name:
+            assert v["regs"] <= 64, (name, v)
+            checked += 1
+    assert checked >= 12
+
+
+def test_sharded_norm_kernels_keep_four_ctas_per_sm(resources):
+    checked = 0
+    for name, v in resources.items():
+        m = re.search(r"qk_norm_kernelILi(\d+)ELi(\d+)E", name)
+        if m and int(m.group(1)) <= 4:
+            assert v["regs"] <= 64, (name, v)
+            checked += 1
+    assert checked >= 6
