@@ -44,6 +44,8 @@
  *   c21 SWIZZLED_8x4 scale-factor tile map (see orc_sf_offset_swizzled_8x4).
  *   c15 partial_norm_out holds the first P columns of n; the RMS is over all H.
  *   c18 QK: rsqrt(V / R + eps), V the fp32 shard-ascending sum of shard means.
+ *   c25 a sum of squares past fp32's range is +inf (fp32 accumulation), so
+ *       rsqrt gives 0 and the norm of such a row is +-0.
  */
 #include <math.h>
 #include <stdint.h>
@@ -299,6 +301,18 @@ enum {
 #define ORC_FP8_BLOCK 128
 #define ORC_FP4_BLOCK 16
 
+/* Mean of squares of n values whose sum of squares ss was accumulated in
+ * double.  The pages accumulate the squares in fp32 (the AMD kernel's
+ * `tl.sum(residual_out * residual_out)`, the var kernel's `tl.sum(x * x)`), so
+ * a sum past the fp32 overflow threshold (2^128 - 2^103, where round-to-
+ * nearest reaches infinity) is +inf; otherwise it is ss / n rounded once. */
+static float mean_of_squares(double ss, double n)
+{
+    if (ss >= ldexp(2.0 - ldexp(1.0, -24), 127))
+        return INFINITY;
+    return (float)(ss / n);
+}
+
 /* Row-wise evaluation of one AllReduceFusionPattern on the rows listed in
  * rows[0..nrows).  Inputs: R partial tensors and the residual, bf16 [*, H]
  * row-major (stride H); gamma bf16 [H].  Outputs are compact, one row per
@@ -382,7 +396,7 @@ static int fused_rows_core(int pattern, int R, const uint16_t *const *partials,
         double ss = 0.0;
         for (int64_t j = 0; j < H; ++j)
             ss += (double)x[j] * (double)x[j];
-        float variance = (float)(ss / (double)H);
+        float variance = mean_of_squares(ss, (double)H);
         float t = variance + eps;
         float scale = (float)(1.0 / sqrt((double)t));
 
@@ -552,8 +566,8 @@ int orc_qk_norm_sharded_rows(int R, const uint16_t *const *shards, int64_t row_s
                 double v = orc_bf16_decode(base[Q + j]);
                 sk += v * v;
             }
-            float vq = (float)(sq / (double)Q);
-            float vk = (float)(sk / (double)K);
+            float vq = mean_of_squares(sq, (double)Q);
+            float vk = mean_of_squares(sk, (double)K);
             Vq = Vq + vq;
             Vk = Vk + vk;
         }
@@ -602,7 +616,7 @@ int orc_rms_norm_sharded_rows(int R, const uint16_t *const *shards, int64_t row_
                 double v = orc_bf16_decode(base[j]);
                 s += v * v;
             }
-            V = V + (float)(s / (double)W);
+            V = V + mean_of_squares(s, (double)W);
         }
         float inv = (float)(1.0 / sqrt((double)(V / (float)R + eps)));
         for (int r = 0; r < R; ++r) {
@@ -632,7 +646,7 @@ static void segment_rmsnorm(const uint16_t *v, int64_t width, const uint16_t *w,
         double d = orc_bf16_decode(v[j]);
         ss += d * d;
     }
-    float var = (float)(ss / (double)width);
+    float var = mean_of_squares(ss, (double)width);
     float s = (float)(1.0 / sqrt((double)(var + eps)));
     for (int64_t j = 0; j < width; ++j) {
         uint16_t b = orc_bf16_encode((orc_bf16_decode(v[j]) * s) * orc_bf16_decode(w[j]));

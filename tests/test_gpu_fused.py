@@ -415,3 +415,23 @@ def test_reducescatter_slices_equal_allreduce_rows(dev):
         assert np.array_equal(host(rso), full["allreduce_out"][start:start + count])
         assert np.array_equal(host(ro), full["residual_out"][start:start + count])
         assert np.array_equal(host(no), full["norm_out"][start:start + count])
+
+
+def test_sum_of_squares_overflow(dev):
+    """Rows whose fp32 sum of squares overflows normalise to +-0 (as the fp32
+    sum on the pages does); a row just below the range keeps its closed form."""
+    R, T, H = 2, 4, 7168
+    vals = np.zeros((R, T, H), np.float32)
+    vals[0, 0] = 1.5e19   # c^2 fits fp32, the sum of 7168 squares does not
+    vals[0, 1] = -1.5e19
+    vals[0, 2] = 1e17     # sum of squares 7.2e37: finite
+    vals[0, 3] = np.random.default_rng(0).standard_normal(H)
+    inp = {"partials": torch.from_numpy(vals).to(torch.bfloat16),
+           "residual": torch.zeros((T, H), dtype=torch.bfloat16),
+           "gamma": torch.full((H,), 1.25, dtype=torch.bfloat16)}
+    for pattern in (1, 6):
+        got = _run_gpu(dev, pattern, inp)
+        want = _oracle(pattern, inp)
+        _compare(pattern, got, want, T=T)
+        if pattern == 1:
+            assert (got["norm_out"][0] == 0x0000).all() and (got["norm_out"][1] == 0x8000).all()

@@ -343,3 +343,21 @@ def test_rejects_bad_shapes(orc):
     gamma = np.zeros(100, np.uint16)
     with pytest.raises(ValueError):
         orc.fused_reduce_norm(6, parts, res, gamma)  # H % 128 != 0
+
+
+def test_sum_of_squares_overflow_follows_fp32(orc):
+    """Reading c25: the squares are summed in fp32 on the pages, so a row whose
+    sum of squares passes fp32's range normalises to +-0; just below the
+    range the closed form holds."""
+    H = 256
+    gamma = bf16_bits_of_f32(np.full(H, 1.25, np.float32))
+    zero = np.zeros((1, H), np.uint16)
+    # c = 1.5e19: c^2 = 2.25e38 fits in fp32 but the sum of 256 squares does not
+    big = bf16_bits_of_f32(np.full((1, H), 1.5e19, np.float32))
+    neg = bf16_bits_of_f32(np.full((1, H), -1.5e19, np.float32))
+    ok = bf16_bits_of_f32(np.full((1, H), 1e17, np.float32))       # 256e34 < 3.4e38
+    assert (orc.fused_reduce_norm(1, [big], zero, gamma)["norm_out"] == 0x0000).all()
+    assert (orc.fused_reduce_norm(1, [neg], zero, gamma)["norm_out"] == 0x8000).all()
+    c = float(f32_of_bf16(ok)[0, 0])
+    want = bf16_of_f64(np.full((1, H), 1.25 * c / np.sqrt(c * c + EPS)))
+    assert np.array_equal(orc.fused_reduce_norm(1, [ok], zero, gamma)["norm_out"], want)

@@ -45,6 +45,7 @@ MUTANTS = {
     "single_matrix_no_div_r": ("(double)(V / (float)R + eps)", "(double)(V + eps)"),
     "single_matrix_weight_slice": ("orc_bf16_decode(weight[r * W + j])", "orc_bf16_decode(weight[j])"),
     "swizzle8_row_stride": ("return tile * 32 + (m % 8) * 4 + (k % 4);", "return tile * 32 + (m % 8) * 3 + (k % 4);"),
+    "no_fp32_overflow": ("    if (ss >= ldexp(2.0 - ldexp(1.0, -24), 127))\n        return INFINITY;\n", ""),
     "ag_block_scale_240": ("float xs = amax / 448.0f;", "float xs = amax / 240.0f;"),
     "ag_y_uses_x_eps": ("segment_rmsnorm(row + q, kv, y_gamma, y_eps,", "segment_rmsnorm(row + q, kv, y_gamma, x_eps,"),
     "ag_y_uses_x_gamma": ("segment_rmsnorm(row + q, kv, y_gamma,", "segment_rmsnorm(row + q, kv, x_gamma,"),
