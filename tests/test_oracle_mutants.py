@@ -24,8 +24,8 @@ MUTANTS = {
                          "x[j] = x[j] + orc_bf16_decode(add_in[in_off + j]);"),
     "token_split_extra_to_last": ("*count = base + (rank < extra ? 1 : 0);",
                                   "*count = base + (rank >= world - extra ? 1 : 0);"),
-    "mean_over_h_minus_1": ("float variance = (float)(ss / (double)H);",
-                            "float variance = (float)(ss / (double)(H - 1));"),
+    "mean_over_h_minus_1": ("float variance = mean_of_squares(ss, (double)H);",
+                            "float variance = mean_of_squares(ss, (double)(H - 1));"),
     "eps_dropped": ("float t = variance + eps;", "float t = variance;"),
     "norm_of_rounded_x": ("float y = (x[j] * scale) * orc_bf16_decode(gamma[j]);",
                           "float y = (orc_bf16_decode(orc_bf16_encode(x[j])) * scale) * orc_bf16_decode(gamma[j]);"),
