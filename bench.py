@@ -383,7 +383,7 @@ def _case_builders():
             return call, fused_bytes(3, 4, T, H, sf_layout=int(layout))
         return build
 
-    def rs_add(rs_pattern):
+    def rs_add(rs_pattern, all_ranks=False):
         def build(dev, stream):
             shape = wl.WORKLOADS["C3"]
             inp = wl.fused_inputs(shape, seed=0, device=dev)
@@ -392,7 +392,7 @@ def _case_builders():
             gen.manual_seed(1)
             add = torch.randn((T, H), generator=gen, device=dev).to(torch.bfloat16)
             calls = []
-            for rank in range(R):
+            for rank in ([-1] if all_ranks else range(R)):
                 start, count = pkg.rs_token_split(T, R, rank)
                 form = 6 if rs_pattern == 7 else 1
                 outs = pkg.new_outputs(form, count, H, dev)
@@ -402,7 +402,7 @@ def _case_builders():
                 for rank, a_in, res, outs in calls:
                     pkg.ts_reducescatter_fused_norm(rs_pattern, inp["partials"], rank, a_in, res, inp["gamma"],
                                                     EPS, launch_with_pdl=True, stream=stream, **outs)
-            return call, rs_add_bytes(R, T, H, rs_pattern == 7)
+            return call, rs_add_bytes(R, T, H, rs_pattern == 7) - (R - 1) * H * 2 * (1 if all_ranks else 0)
         return build
 
     def ag(pattern):
@@ -465,6 +465,7 @@ def _case_builders():
         "c4-p3-swizzled": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF SWIZZLED_128x4", c4(0)),
         "c4-p3-swizzled8": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF SWIZZLED_8x4", c4(1)),
         "rs-add": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls)", rs_add(8)),
+        "rs-add-all": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, rank -1 (one call)", rs_add(8, True)),
         "rs-add-fp8b": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls)",
                         rs_add(7)),
         "ag-rms": ("kAllGatherfusedRMS R=8 T=65536 1536|512|64", ag(1)),

@@ -217,7 +217,8 @@ typedef enum {
  *                 0..6 on the slice; 7 = 6 with add_in; 8 = 1 with add_in.
  *   partials      host array of R device pointers, each bf16 [T, H] (all T
  *                 tokens; only the slice's rows are read).
- *   rank          0..R-1.
+ *   rank          0..R-1, or -1 for every rank's slice in one launch (the
+ *                 slices in rank order are all T tokens: count = T, start = 0).
  *   add_in        bf16 [count, H]; required for codes 7 and 8, NULL otherwise.
  *   residual      bf16 [count, H] (the slice's rows; codes 1..8).
  *   outs          outputs with count rows (partial_norm_out must be NULL).

@@ -256,7 +256,10 @@ def ts_fused_reduce_norm(pattern: int, partials, residual: torch.Tensor | None =
 
 def rs_token_split(T: int, world: int, rank: int) -> tuple[int, int]:
     """(start, count) of rank ``rank``'s token slice: T//world tokens each, the
-    first T % world ranks one more (tokenspeed triton.py `rsag_get_token_dist`)."""
+    first T % world ranks one more (tokenspeed triton.py `rsag_get_token_dist`).
+    Rank -1 stands for every rank's slice: (0, T)."""
+    if rank < 0:
+        return 0, T
     base, extra = divmod(T, world)
     return rank * base + min(rank, extra), base + (1 if rank < extra else 0)
 
@@ -275,7 +278,8 @@ def ts_reducescatter_fused_norm(rs_pattern: int, partials, rank: int, add_in: to
 
     ``partials``: R CUDA bf16 tensors [T, H] holding every token; ``add_in``,
     ``residual`` and the outputs have the rank's ``count`` rows
-    (``rs_token_split(T, R, rank)``).
+    (``rs_token_split(T, R, rank)``); ``rank=-1`` computes every rank's slice
+    in one launch (all T rows).
     """
     parts = [_dev(p, "partials[%d]" % i, torch.bfloat16) for i, p in enumerate(_rows(partials, "partials"))]
     T, H = parts[0].shape

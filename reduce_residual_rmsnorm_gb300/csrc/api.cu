@@ -298,16 +298,17 @@ extern "C" int ts_reducescatter_fused_norm(int rs_pattern, const void *const *pa
         return fail(TS_ERR_NULL, "partials is NULL");
     if (R < 1 || R > tsfn::kMaxR)
         return fail(TS_ERR_SHAPE, "R = %d outside 1..%d", R, tsfn::kMaxR);
-    if (rank < 0 || rank >= R)
-        return fail(TS_ERR_SHAPE, "rank = %d outside 0..R-1 (R = %d)", rank, R);
+    if (rank < -1 || rank >= R)
+        return fail(TS_ERR_SHAPE, "rank = %d outside -1..R-1 (R = %d)", rank, R);
     if (T < 0 || T > kMaxRows)
         return fail(TS_ERR_SHAPE, "T = %lld outside 0..%lld", (long long)T, (long long)kMaxRows);
     if (H < 8 || H % 8 != 0)
         return fail(TS_ERR_SHAPE, "H = %lld must be a positive multiple of 8", (long long)H);
-    // token slice of `rank` (T/R each, the first T%R ranks one more)
+    // token slice of `rank` (T/R each, the first T%R ranks one more); rank -1:
+    // every rank's slice, which in rank order is all T tokens
     const int64_t base = T / R, extra = T % R;
-    const int64_t count = base + (rank < extra ? 1 : 0);
-    const int64_t start = rank * base + (rank < extra ? rank : extra);
+    const int64_t count = rank < 0 ? T : base + (rank < extra ? 1 : 0);
+    const int64_t start = rank < 0 ? 0 : rank * base + (rank < extra ? rank : extra);
     const void *sliced[tsfn::kMaxR];
     for (int r = 0; r < R; ++r) {
         if (partials[r] == nullptr && T > 0)

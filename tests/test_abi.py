@@ -321,12 +321,13 @@ def _rs_call(lib, rs=8, R=4, rank=0, T=16, H=256, add=True, flags=0, mutate=None
 
 def test_rs_valid_empty_calls(lib):
     assert _rs_call(lib, T=0)[0] == TS_OK
+    assert _rs_call(lib, T=0, rank=-1)[0] == TS_OK
     assert _rs_call(lib, T=2, R=4, rank=3)[0] == TS_OK  # rank 3 of 4 owns no token of 2
 
 
 NEG_RS = [
     ("rs pattern 9", dict(rs=9), BAD_PATTERN),
-    ("rank -1", dict(rank=-1), SHAPE),
+    ("rank -2", dict(rank=-2), SHAPE),
     ("rank == R", dict(rank=4), SHAPE),
     ("add_in missing for 8", dict(add=False), NULL),
     ("add_in missing for 7", dict(rs=7, add=False), NULL),

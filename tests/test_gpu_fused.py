@@ -435,3 +435,23 @@ def test_sum_of_squares_overflow(dev):
         _compare(pattern, got, want, T=T)
         if pattern == 1:
             assert (got["norm_out"][0] == 0x0000).all() and (got["norm_out"][1] == 0x8000).all()
+
+
+def test_reducescatter_all_ranks_in_one_launch(dev):
+    """rank = -1: every rank's slice in one launch equals the per-rank calls."""
+    R, T, H = 8, 1000, 7168
+    inp = _inputs(R, T, H, seed=13)
+    g = torch.Generator().manual_seed(5)
+    add = torch.randn((T, H), generator=g).to(torch.bfloat16).to(dev)
+    parts, res, gamma = inp["partials"].to(dev), inp["residual"].to(dev), inp["gamma"].to(dev)
+    for rs, form in ((8, 1), (7, 6)):
+        whole = pkg.new_outputs(form, T, H, dev)
+        pkg.ts_reducescatter_fused_norm(rs, parts, -1, add, res, gamma, EPS, **whole)
+        for rank in range(R):
+            start, count = pkg.rs_token_split(T, R, rank)
+            one = pkg.new_outputs(form, count, H, dev)
+            pkg.ts_reducescatter_fused_norm(rs, parts, rank, add[start:start + count], res[start:start + count],
+                                            gamma, EPS, **one)
+            torch.cuda.synchronize()
+            for k, v in one.items():
+                assert np.array_equal(host(v), host(whole[k][start:start + count])), (rs, rank, k)
