@@ -260,6 +260,59 @@ def oracle_rows_per_second(inp_host: dict, seconds: float, pattern: int = 1):
             return done / el, done, el
 
 
+def _oracle_worker(args):
+    """One process of the all-cores baseline: memory-map the bf16 inputs the
+    parent wrote, then run the oracle on this worker's rows for ``seconds``."""
+    path, R, T, H, first, stride, seconds = args
+    import numpy as np
+
+    import oracle
+
+    data = np.memmap(path, dtype=np.uint16, mode="r", shape=(R + 1, T, H))
+    gamma = np.memmap(path + ".gamma", dtype=np.uint16, mode="r", shape=(H,))
+    parts = [np.asarray(data[r]) for r in range(R)]
+    res = np.asarray(data[R])
+    gamma = np.asarray(gamma)
+    done, row, start = 0, first, time.perf_counter()
+    while True:
+        rows = (np.arange(8) * stride + row) % T
+        oracle.fused_reduce_norm(1, parts, res, gamma, EPS, rows=rows)
+        done += 8
+        row = (row + 8 * stride) % T
+        el = time.perf_counter() - start
+        if el >= seconds:
+            return done, el
+
+
+def oracle_rows_per_second_all_cores(inp_host: dict, seconds: float):
+    """The same oracle, one spawned process per host core, each on its own rows
+    (a reported baseline only); returns (rows/s, cores)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    import tempfile
+
+    import numpy as np
+
+    from reduce_residual_rmsnorm_gb300 import workloads as wl
+
+    cores = os.cpu_count() or 1
+    R, T, H = inp_host["partials"].shape
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "inputs.bf16")
+        mm = np.memmap(path, dtype=np.uint16, mode="w+", shape=(R + 1, T, H))
+        for r in range(R):
+            mm[r] = wl.bits(inp_host["partials"][r])
+        mm[R] = wl.bits(inp_host["residual"])
+        mm.flush()
+        del mm
+        wl.bits(inp_host["gamma"]).tofile(path + ".gamma")
+        # spawned (not forked) workers; a worker that dies raises instead of hanging
+        with cf.ProcessPoolExecutor(cores, mp_context=mp.get_context("spawn")) as ex:
+            futs = [ex.submit(_oracle_worker, (path, R, T, H, i, cores, seconds)) for i in range(cores)]
+            res = [f.result(timeout=seconds + 300) for f in futs]
+    return sum(done / el for done, el in res), cores
+
+
 # ---------------------------------------------------------------------------
 # the reference arm: the oracle on host cores
 # ---------------------------------------------------------------------------
@@ -606,12 +659,17 @@ def run_ours(args):
     if not args.no_rows:
         rows = measure_rows(dev, stream, peak, args.row_iters)
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         rps, done, el = oracle_rows_per_second(host_inp, args.cpu_seconds)
         cpu = {"value": rps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{done} rows of the R=8 T=4096 H=7168 kARResidualRMSNorm workload "
                          f"(8-row batches, wrapping), {el:.1f} s of single-threaded C"}
+        if args.cpu_all_cores:
+            rps_all, cores = oracle_rows_per_second_all_cores(host_inp, args.cpu_seconds)
+            cpu_all = {"value": rps_all, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                       "sample": f"one spawned process per core, each {args.cpu_seconds:.0f} s on its own rows "
+                                 f"of the same workload"}
 
     if rank == 0:
         line = {
@@ -629,6 +687,7 @@ def run_ours(args):
             "e2e": {"value": T * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
             "gpu_launches": args.steps,
             "clocks": sampler.summary(),
             "kernel_source_hash": kernel_source_hash(),
@@ -646,6 +705,8 @@ def main(argv=None):
     ap.add_argument("--no-rows", action="store_true", help="skip the other patterns/workloads")
     ap.add_argument("--row-iters", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-all-cores", dest="cpu_all_cores", action="store_false",
+                    help="skip the all-cores oracle baseline")
     ap.add_argument("--profile-case", default=None,
                     help="only set up this named workload and launch it --launches times (for ncu)")
     ap.add_argument("--launches", type=int, default=3)
