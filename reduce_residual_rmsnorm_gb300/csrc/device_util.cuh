@@ -31,31 +31,35 @@ __device__ __forceinline__ uint4 ld_keep(const void *p)
     return v;
 }
 
+// Outputs are stored with the streaming (evict-first) hint: each is written
+// once and read by a later kernel, and keeping a step's ~100 MB of dirty
+// output lines from crowding L2 measured 3 % faster on the R=8 T=4096 H=7168
+// step (92.8 us vs 96.0 us).
 __device__ __forceinline__ void st_v4(void *p, uint4 v)
 {
-    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
                  : "memory");
 }
 
 __device__ __forceinline__ void st_v2(void *p, uint2 v)
 {
-    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+    asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
 __device__ __forceinline__ void st_u32(void *p, uint32_t v)
 {
-    asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void st_u8(void *p, uint32_t v)
 {
-    asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+    asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void st_f32(void *p, float v)
 {
-    asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+    asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------
