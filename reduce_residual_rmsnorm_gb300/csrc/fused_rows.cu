@@ -5,9 +5,10 @@
 // (and `amd_all_reduce_kernel` for kAllReduce): the R partials are widened to
 // fp32 and added in ascending order into an accumulator that starts at +0,
 // the optional add_in of the reduce-scatter "Add" patterns (trtllm.py
-// `ReduceScatterFusionPattern`) and then the residual are added in fp32, the row's mean of squares of that unrounded
-// fp32 x gives s = rsqrt(mean + eps), and n = bf16((x * s) * gamma).  The
-// quantisers of trtllm.py `AllReduceFusionPattern` then read n:
+// `ReduceScatterFusionPattern`) and then the residual are added in fp32, the
+// row's mean of squares of that unrounded fp32 x gives s = rsqrt(mean + eps),
+// and n = bf16((x * s) * gamma).  The quantisers of trtllm.py
+// `AllReduceFusionPattern` then read n:
 //   FP8 per tensor   code = e4m3(n * sigma)
 //   FP8 1x128 block  s_g = amax/448, code = e4m3(n / s_g)  (0 if s_g == 0)
 //   NVFP4 16-block   SF = e4m3(g * (amax/6)), code = e2m1(n * (g / value(SF)))
@@ -32,8 +33,8 @@ constexpr int kMaxThreads = 512;
 // every cap <= 128 keeps a full CTA launchable): at most 8 partials and 2
 // chunks per thread must leave room for two 512-thread CTAs per SM (64
 // registers), and with at most 4 partials (no add_in) for four 320-thread
-// CTAs (48; registers are allocated in steps of 8 per thread).  The tests check that no
-// instance spills.
+// CTAs (48; registers are allocated in steps of 8 per thread).  The tests
+// check that no instance spills.
 template <int RB, int V, bool ADD>
 constexpr int reg_cap()
 {
