@@ -120,17 +120,43 @@ def read_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = ("fused_rows.cu", "qk_norm.cu", "device_util.cuh", "launch.h", "sf_layout.cuh")
+KERNEL_SOURCES = ("ag_norm.cu", "device_util.cuh", "fused_rows.cu", "launch.h", "qk_norm.cu", "sf_layout.cuh")
+
+
+def _code_tokens(text: str) -> str:
+    """C/C++ source with comments removed and whitespace runs collapsed, so
+    that rewording a comment does not change the hash (string and character
+    literals are kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif text[i] in "\"'":
+            j = i + 1
+            while j < n and text[j] != text[i]:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return " ".join("".join(out).split())
 
 
 def kernel_source_hash() -> str:
-    """Hash of the device-code sources (not the host-side argument checks)."""
+    """Hash of the device code (not the host-side argument checks), comments
+    and layout excluded."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "reduce_residual_rmsnorm_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
         if fn in KERNEL_SOURCES:
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, fn), encoding="utf-8") as f:
+                h.update(fn.encode() + b"\0" + _code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,0 +1,125 @@
+"""Host-side logic of the benchmark: the algorithmic byte counts behind every
+roofline fraction, and the source hash that ties a recorded ncu traffic figure
+to the kernels it was taken on.
+
+The byte counts are checked against tensor-by-tensor lists written out here
+(every input read once, every output written once, with element sizes bf16 2,
+e4m3 1, e2m1 1/2, fp32 4, e4m3 scale factor 1), so that a dropped or doubled
+tensor in the formulas shows up.
+"""
+import json
+import os
+
+import pytest
+
+import bench
+
+R, T, H = 8, 4096, 7168
+
+
+def _nbytes(*tensors):
+    total = 0
+    for shape, size in tensors:
+        n = 1
+        for d in shape:
+            n *= d
+        total += n * size
+    return int(total)
+
+
+def test_headline_bytes():
+    want = _nbytes(*[((T, H), 2)] * R,         # partials
+                   ((T, H), 2), ((H,), 2),     # residual, gamma
+                   ((T, H), 2), ((T, H), 2))   # residual_out, norm_out
+    assert bench.fused_bytes(1, R, T, H) == want
+    # with the optional allreduce_out as well
+    assert bench.fused_bytes(1, R, T, H, allreduce_out=True) == want + T * H * 2
+
+
+def test_allreduce_only_bytes():
+    assert bench.fused_bytes(0, R, T, H) == _nbytes(*[((T, H), 2)] * R, ((T, H), 2))
+
+
+@pytest.mark.parametrize("pattern", range(2, 9))
+def test_quantising_pattern_bytes(pattern):
+    P = 1024
+    reads = [((T, H), 2)] * R + [((T, H), 2), ((H,), 2)]
+    writes = [((T, H), 2)]  # residual_out
+    if pattern in (2, 3, 4, 5):
+        reads.append(((1,), 4))  # the global scale factor
+    if pattern in (4, 5):
+        writes.append(((T, H), 2))  # norm_out
+    if pattern in (7, 8):
+        writes.append(((T, P), 2))  # partial_norm_out
+    if pattern in (2, 4):
+        writes.append(((T, H), 1))
+    if pattern in (6, 7):
+        writes += [((T, H), 1), ((T, H // 128), 4)]
+    if pattern in (3, 5):
+        writes += [((T, H), 0.5), ((T, H // 16), 1)]  # LINEAR scale factors
+    assert bench.fused_bytes(pattern, R, T, H, P=P) == _nbytes(*reads, *writes)
+
+
+@pytest.mark.parametrize("layout,rows", [(0, 128), (1, 40)])
+def test_swizzled_scale_factor_padding_is_counted(layout, rows):
+    """T=37, H=320: 20 scale factors per row padded to 20 columns; rows padded
+    to the 128- or 8-row tile."""
+    t, h = 37, 320
+    base = bench.fused_bytes(3, 2, t, h, sf_layout=2) - t * (h // 16)
+    assert bench.fused_bytes(3, 2, t, h, sf_layout=layout) == base + rows * 20
+
+
+def test_sharded_norm_bytes():
+    Q, K = 1024, 128
+    assert bench.qk_bytes(R, T, Q, K) == _nbytes(((T, R * (Q + K)), 2), ((T, R * (Q + K)), 2),
+                                                 ((R * (Q + K),), 2))
+    assert bench.rms_sharded_bytes(R, T, 768) == _nbytes(((T, R * 768), 2), ((T, R * 768), 2), ((R * 768,), 2))
+
+
+def test_reduce_scatter_bytes_over_all_ranks():
+    """R calls, one per rank's slice: each partial row read once, add_in and
+    residual once, gamma once per call."""
+    want = _nbytes(*[((T, H), 2)] * R, ((T, H), 2), ((T, H), 2), ((R, H), 2),
+                   ((T, H), 2), ((T, H), 2))
+    assert bench.rs_add_bytes(R, T, H) == want
+    want8 = want - T * H * 2 + _nbytes(((T, H), 1), ((T, H // 128), 4))
+    assert bench.rs_add_bytes(R, T, H, fp8_block=True) == want8
+
+
+def test_allgather_bytes():
+    t, q, kv, rope = 65536, 1536, 512, 64
+    hid = q + kv + rope
+    assert bench.ag_bytes(0, t, q, kv, rope) == _nbytes(((t, hid), 2), ((t, hid), 2))
+    assert bench.ag_bytes(1, t, q, kv, rope) == _nbytes(((t, hid), 2), ((t, hid), 2), ((t, q), 2), ((t, kv), 2),
+                                                        ((q,), 2), ((kv,), 2))
+    assert bench.ag_bytes(2, t, q, kv, rope) == _nbytes(((t, hid), 2), ((t, hid), 2), ((t, kv), 2), ((t, q), 1),
+                                                        ((t, q // 128), 4), ((q,), 2), ((kv,), 2))
+
+
+def test_roofline_entry_arithmetic():
+    e = bench.roofline_entry(7_000_000_000, 1.0, 7000.0)
+    assert e["gbs"] == pytest.approx(7000.0) and e["frac"] == pytest.approx(1.0) and e["us"] == 1000.0
+
+
+def test_code_tokens_ignore_comments_and_layout():
+    a = "int f(int x) {\n  // doubles x\n  return 2 * x; /* ok */\n}\n"
+    b = "int f(int x)\n{\n    /* twice x,\n       as before */ return 2 * x;\n}"
+    assert bench._code_tokens(a) == bench._code_tokens(b)
+    assert bench._code_tokens(a) != bench._code_tokens(a.replace("2 * x", "3 * x"))
+
+
+def test_code_tokens_keep_literals():
+    src = 'asm("ld.global.cs.v4.u32 {%0}, [%1]; // not a comment"); char c = \'"\'; // gone'
+    out = bench._code_tokens(src)
+    assert "// not a comment" in out and "gone" not in out and "'\"'" in out
+
+
+def test_recorded_traffic_table_is_well_formed():
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    for h, cap in rec["captures"].items():
+        assert len(h) == 16 and int(h, 16) >= 0
+        for prof in cap["profile"].split(", "):
+            assert os.path.exists(os.path.join(bench.ROOT, "profiles", prof)), prof
+        for key, v in cap["bytes_per_launch"].items():
+            assert isinstance(v, int) and v > 0, key
