@@ -11,7 +11,12 @@
 // One warp per gathered row (rows are at most 2112 wide: 264 chunks of 8, at
 // most 9 per lane), 8 rows per CTA.  The row stays in registers as packed
 // bf16; q_lora_rank % 128 == 0 puts the x/y boundary on a half-warp boundary,
-// so the 16-lane shuffles of an FP8 block never mix x with y.
+// so the 16-lane shuffles of an FP8 block never mix x with y.  The FP8 form of
+// a 2112-wide row needs a few more than the 64 registers that four CTAs per SM
+// allow, and ptxas spills 3 of them to local memory: measured on the R=8,
+// T=65536, 1536 | 512 | 64 workload this beats every spill-free arrangement
+// (115.0 us against 122.2 us with the x norms parked in shared memory for a
+// second pass, 123.8 us at 3 CTAs per SM, 133.3 us with two warps per row).
 #include "device_util.cuh"
 #include "launch.h"
 
@@ -114,8 +119,9 @@ __global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_norm_kernel(const __gr
                 st_v4(a.y_norm_out + t * a.kv + (int64_t)(c - qc) * 8, nb);
             }
         }
-        if constexpr (PATTERN == 2) {
-            // 16 lanes = one 128-column block of x; every lane takes part
+        if (PATTERN == 2 && 32 * i < qc) {
+            // 16 lanes = one 128-column block of x; every lane of the warp
+            // takes part (x may end half-way through the warp)
             float amax = 0.0f;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -127,15 +133,8 @@ __global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_norm_kernel(const __gr
                 const float sg = __fdiv_rn(amax, 448.0f);
                 if ((c & 15) == 0)
                     st_f32(a.scale_out + t * (a.q >> 7) + (c >> 4), sg);
-                uint2 codes = make_uint2(0, 0);
-                if (sg != 0.0f) {
-                    float q[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        q[e] = __fdiv_rn(nf[e], sg);
-                    codes = cvt_e4m3x8(q);
-                }
-                st_v2(a.quant_out + t * a.q + (int64_t)c * 8, codes);
+                st_v2(a.quant_out + t * a.q + (int64_t)c * 8,
+                      sg != 0.0f ? e4m3_block_codes(nf, sg) : make_uint2(0, 0));
             }
         }
     }

@@ -146,6 +146,38 @@ __device__ __forceinline__ float e4m3_value(uint32_t c)
     return (c & 0x80u) ? -mag : mag;
 }
 
+// E4M3 codes of the quotients n[i] / s of one FP8 1x128 block, s = amax/448
+// (amax the block's largest |n|, s > 0), for bf16-valued n, without a divide
+// per element.
+//
+// Each quotient is q0 = RN(n r) from the correctly rounded reciprocal
+// r = RN(1/s), with one remainder correction q = RN(q0 - RN(q0 s - n) r), the
+// remainder taken by a fused multiply-add (Markstein's correction, IBM J. Res.
+// Develop. 34(1), 1990).  A scale s below 2^-112 is first multiplied, with n,
+// by 2^64 (exact: both are powers-of-two shifts), so that 1/s stays finite;
+// for s = +inf the remainder term is dropped, leaving q = RN(n * 0) (a signed
+// zero, or NaN for an infinite n, as the IEEE quotient).  Over every pair of
+// bf16 values n, amax with |n| <= amax this gives the E4M3 code of the
+// correctly rounded quotient n / s; the quotient itself can differ from it in
+// the last fp32 bit only where n is so small that the code is 0 either way.
+// A sweep of the whole domain on the GPU checks the codes against the IEEE
+// divide.
+__device__ __forceinline__ uint2 e4m3_block_codes(const float (&n)[8], float s)
+{
+    const float k = s < 0x1p-112f ? 0x1p64f : 1.0f;
+    const float sk = __fmul_rn(s, k);
+    const float r = __frcp_rn(sk);
+    const float sr = sk <= 0x1.fffffep127f ? sk : 0.0f;
+    float q[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float nk = __fmul_rn(n[e], k);
+        const float q0 = __fmul_rn(nk, r);
+        q[e] = __fmaf_rn(-__fmaf_rn(q0, sr, -nk), r, q0);
+    }
+    return cvt_e4m3x8(q);
+}
+
 // ---------------------------------------------------------------------------
 // programmatic dependent launch
 // ---------------------------------------------------------------------------

@@ -193,15 +193,7 @@ __global__ void __maxnreg__((reg_cap<RB, V, ADD>()))
             if (live) {
                 if ((c & 15) == 0)
                     st_f32(static_cast<float *>(a.scale_out) + row * (a.H >> 7) + (c >> 4), sg);
-                uint2 codes = make_uint2(0, 0);
-                if (sg != 0.0f) {
-                    float q[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        q[e] = __fdiv_rn(nf[e], sg);
-                    codes = cvt_e4m3x8(q);
-                }
-                st_v2(a.quant_out + off, codes);
+                st_v2(a.quant_out + off, sg != 0.0f ? e4m3_block_codes(nf, sg) : make_uint2(0, 0));
             }
         } else if constexpr (EP == Epilogue::kFp4) {
             float amax = 0.0f;

@@ -1,6 +1,8 @@
 // Test-only probe: applies the library's conversion helpers (device_util.cuh)
 // to arbitrary fp32 inputs so the GPU conversions can be compared with the
-// oracle's encoders on exhaustive sweeps.  Built by tests/test_gpu_cvt.py.
+// oracle's encoders on exhaustive sweeps, and sweeps the FP8 1x128 block
+// quotient over its whole bf16 domain against the IEEE divide.  Built by
+// tests/test_gpu_cvt.py.
 #include <cstdint>
 
 #include "device_util.cuh"
@@ -35,6 +37,36 @@ __global__ void e4m3_value_kernel(float *out)
         out[c] = tsfn::e4m3_value(c);
 }
 
+// Block blockIdx.x takes amax = the bf16 pattern blockIdx.x + 1 (every
+// positive value up to +inf), s = amax/448 as the kernels form it, and every
+// bf16 n with |n| <= amax: the E4M3 codes of tsfn::e4m3_block_codes against
+// the codes of the IEEE quotients; mismatches counted per amax pattern.
+__global__ void block_codes_kernel(uint32_t *mismatch)
+{
+    const uint32_t ab = blockIdx.x + 1;
+    const float amax = __uint_as_float(ab << 16);
+    const float s = __fdiv_rn(amax, 448.0f);
+    uint32_t bad = 0;
+    for (uint32_t g = threadIdx.x; g < 8192; g += blockDim.x) {
+        float n[8], qd[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            n[e] = __uint_as_float((g * 8 + e) << 16);
+            qd[e] = __fdiv_rn(n[e], s);
+        }
+        const uint2 got = tsfn::e4m3_block_codes(n, s), want = tsfn::cvt_e4m3x8(qd);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t gw = e < 4 ? got.x : got.y, ww = e < 4 ? want.x : want.y;
+            const int sh = 8 * (e & 3);
+            if (fabsf(n[e]) <= amax && ((gw >> sh) & 0xFFu) != ((ww >> sh) & 0xFFu))
+                ++bad;
+        }
+    }
+    if (bad)
+        atomicAdd(&mismatch[ab], bad);
+}
+
 }  // namespace
 
 extern "C" __attribute__((visibility("default"))) int cvt_probe(const float *x, int64_t n, uint16_t *bf16_out, uint8_t *e4m3_out, uint8_t *e2m1_out)
@@ -50,5 +82,13 @@ extern "C" __attribute__((visibility("default"))) int cvt_probe(const float *x, 
 extern "C" __attribute__((visibility("default"))) int e4m3_values(float *out)
 {
     e4m3_value_kernel<<<1, 256>>>(out);
+    return (int)cudaGetLastError();
+}
+
+// mismatch: 0x7F81 counters, zeroed by the caller; entry a counts the bf16 n
+// whose block-quotient code differs from the IEEE one for amax pattern a.
+extern "C" __attribute__((visibility("default"))) int block_codes_probe(uint32_t *mismatch)
+{
+    block_codes_kernel<<<0x7F80, 256>>>(mismatch);
     return (int)cudaGetLastError();
 }

@@ -66,6 +66,9 @@ CASES = [  # R, T, q, kv, rope
     (4, 2, 256, 128, 64),      # ranks 2 and 3 own no token
     (2, 33, 512, 256, 32),
     (16, 100, 1024, 512, 64),
+    (3, 7, 1408, 512, 64),     # x ends mid-warp (176 chunks); the last CTA part empty
+    (5, 13, 1024, 8, 0),       # just past 4 chunks per lane
+    (2, 5, 384, 1024, 8),      # x ends mid-warp, y wider than x
 ]
 
 
@@ -105,6 +108,26 @@ def test_fp8_without_x_norm_out(dev):
 
 
 @pytest.mark.slow
+def test_fp8_block_scales_across_the_range(dev):
+    """x_gamma per 128-column block from 2^-130 to 2^100: block scales that are
+    fp32 subnormals, below 2^-112 and large, in one row."""
+    full, slices, xg, yg = _inputs(4, 9, 1024, 128, 64, seed=12)
+    mult = torch.tensor([2.0 ** -130, 2.0 ** -118, 2.0 ** -112, 1.0, 2.0 ** 40, 2.0 ** 100, 2.0 ** -2, 3.0])
+    xg = (xg.float() * mult.repeat_interleave(128)).to(torch.bfloat16)
+    got = _run(dev, 2, slices, 1024, 128, 64, xg, yg)
+    want = oracle.allgather_fused_norm(2, [wl.bits(s) for s in slices], 1024, 128, wl.bits(xg), wl.bits(yg))
+    assert_bf16_close(got["x_norm_out"], want["x_norm_out"], 1, 0.999, "x_norm")
+    codes_close(got["quant_out"], want["quant_out"], e4m3_order, 1, 1e-4, "x e4m3")
+    n = f32_of_bf16(got["x_norm_out"]).reshape(9, 8, 128)
+    s = np.abs(n).max(-1).astype(np.float32) / np.float32(448.0)
+    assert np.array_equal(got["scale_out"], s)
+    assert (s[:, 0] < 2.0 ** -126).all() and (s[:, 1] < 2.0 ** -112).all()
+    with np.errstate(divide="ignore", invalid="ignore"):
+        codes = oracle.e4m3_encode((n / s[..., None]).astype(np.float32)).reshape(9, 1024)
+    codes[np.repeat(s == 0, 128, axis=-1).reshape(9, 1024)] = 0
+    assert np.array_equal(got["quant_out"], codes)
+
+
 def test_full_size(dev):
     """R=8, T=65536 gathered tokens of 1536 | 512 | 64: sampled rows."""
     full, slices, xg, yg = _inputs(8, 65536, 1536, 512, 64, seed=0)

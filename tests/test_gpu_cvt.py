@@ -3,7 +3,10 @@ and .e2m1x2, and the E4M3 decoder used for NVFP4 scale factors), driven
 directly through a test-only probe kernel, equal the oracle's encoders on an
 exhaustive sweep: every finite bf16 value at several scales, every rounding
 midpoint of each format and its neighbours, zeros of both signs, subnormals,
-values past saturation and a million random fp32 bit patterns."""
+values past saturation and a million random fp32 bit patterns.  The FP8 1x128
+block quantiser's divide-free quotient gives the E4M3 code of the IEEE quotient
+over its whole domain (every positive bf16 amax up to +inf, every bf16 n with
+|n| <= amax)."""
 import ctypes
 import os
 import subprocess
@@ -31,6 +34,8 @@ def probe(tmp_path_factory):
     lib.cvt_probe.restype = ctypes.c_int
     lib.e4m3_values.argtypes = [ctypes.c_void_p]
     lib.e4m3_values.restype = ctypes.c_int
+    lib.block_codes_probe.argtypes = [ctypes.c_void_p]
+    lib.block_codes_probe.restype = ctypes.c_int
     return lib
 
 
@@ -86,3 +91,11 @@ def test_e4m3_decoder_matches_the_oracle(probe):
     want = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
     fin = np.isfinite(want)  # 0x7F / 0xFF are NaN codes, never produced by a saturating cvt
     assert np.array_equal(got[fin].view(np.uint32), want[fin].view(np.uint32))
+
+
+def test_block_quotient_codes_equal_the_ieee_divide_everywhere(probe):
+    mism = torch.zeros(0x7F81, dtype=torch.int32, device="cuda:0")
+    assert probe.block_codes_probe(mism.data_ptr()) == 0
+    torch.cuda.synchronize()
+    bad = mism.cpu().numpy()
+    assert bad.sum() == 0, {hex(int(a)): int(bad[a]) for a in np.nonzero(bad)[0][:10]}

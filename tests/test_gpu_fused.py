@@ -208,6 +208,25 @@ def test_saturation_and_extremes(dev):
     _compare(3, got, _oracle(3, inp, 1.0e6), T=T)
 
 
+@pytest.mark.parametrize("pattern", [6, 7])
+def test_fp8_blockwise_block_scales_across_the_range(dev, pattern):
+    """gamma per 128-column block from 2^-130 (block scales that are fp32
+    subnormals) through 2^-118 (scales below 2^-112) to 2^100, so that blocks
+    of one row take every branch of the divide-free block quotient."""
+    R, T, H = 3, 11, 1024
+    inp = _inputs(R, T, H, seed=11)
+    mult = torch.tensor([2.0 ** -130, 2.0 ** -118, 2.0 ** -112, 2.0 ** -100, 1.0, 2.0 ** 40, 2.0 ** 100, 2.0 ** -2])
+    inp["gamma"] = (inp["gamma"].float() * mult.repeat_interleave(128)).to(torch.bfloat16)
+    P = 256 if pattern == 7 else 0
+    base = _run_gpu(dev, 1, inp)
+    got = _run_gpu(dev, pattern, inp, None, P)
+    _compare(pattern, got, _oracle(pattern, inp, 0.0, P), T=T)
+    got["norm_ref"] = base["norm_out"]
+    _self_consistency(pattern, got, None)
+    s = got["scale_out"]
+    assert (s[:, 0] < 2.0 ** -126).all() and (s[:, 1] < 2.0 ** -112).all() and (s[:, 6] > 2.0 ** 90).all()
+
+
 def test_in_place_allreduce_and_residual(dev):
     R, T, H = 4, 33, 1024
     inp = _inputs(R, T, H, seed=8)
