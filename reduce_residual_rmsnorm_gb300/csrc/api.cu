@@ -33,6 +33,17 @@ int ok()
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// 1/n when n (>= 1) is a power of two, which fp32 holds exactly; else 0.
+float pow2_reciprocal(int64_t n)
+{
+    if (n <= 0 || (n & (n - 1)) != 0)
+        return 0.0f;
+    float r = 1.0f;
+    for (int64_t m = n; m > 1; m >>= 1)
+        r *= 0.5f;
+    return r;
+}
+
 struct Span {
     uintptr_t lo = 0, hi = 0;  // [lo, hi)
     const char *name = "";
@@ -395,6 +406,9 @@ int sharded_norm(const char *what, const void *const *shards, int R, int64_t T, 
     a.row_stride = row_stride;
     a.Q = (int)Q;
     a.K = (int)K;
+    a.inv_q = pow2_reciprocal(Q);
+    a.inv_k = pow2_reciprocal(K);
+    a.inv_r = pow2_reciprocal(R);
     a.q_weight = static_cast<const uint16_t *>(q_weight);
     a.k_weight = has_k ? static_cast<const uint16_t *>(k_weight) : nullptr;
     a.eps = eps;

@@ -54,6 +54,9 @@ struct QKArgs {
     int64_t row_stride;
     int Q;
     int K;
+    // 1/Q, 1/K, 1/R where that count is a power of two (exact), else 0: the
+    // kernel then multiplies instead of dividing, with the same rounded result
+    float inv_q, inv_k, inv_r;
     const uint16_t *q_weight;
     const uint16_t *k_weight;
     float eps;
