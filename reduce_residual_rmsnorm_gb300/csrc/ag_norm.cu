@@ -12,11 +12,12 @@
 // most 9 per lane), 8 rows per CTA.  The row stays in registers as packed
 // bf16; q_lora_rank % 128 == 0 puts the x/y boundary on a half-warp boundary,
 // so the 16-lane shuffles of an FP8 block never mix x with y.  The FP8 form of
-// a 2112-wide row needs a few more than the 64 registers that four CTAs per SM
-// allow, and ptxas spills 3 of them to local memory: measured on the R=8,
-// T=65536, 1536 | 512 | 64 workload this beats every spill-free arrangement
-// (115.0 us against 122.2 us with the x norms parked in shared memory for a
-// second pass, 123.8 us at 3 CTAs per SM, 133.3 us with two warps per row).
+// a 2112-wide row fits the 64 registers that four CTAs per SM allow.  On the
+// R=8, T=65536, 1536 | 512 | 64 workload this single-warp arrangement beat
+// the others measured, even while it still spilled 3 registers: 115.0 us
+// against 122.2 us with the x norms parked in shared memory for a second
+// pass, 123.8 us at 3 CTAs per SM and 133.3 us with two warps per row (it
+// now takes 111.2 us, without spilling).
 #include "device_util.cuh"
 #include "launch.h"
 
@@ -37,20 +38,20 @@ __global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_norm_kernel(const __gr
     if (t >= a.T)
         return;
 
-    // which rank's slice holds gathered row t
-    const int64_t base = a.T / a.R, extra = a.T % a.R;
-    int rank;
-    int64_t local;
-    if (t < extra * (base + 1)) {
-        rank = (int)(t / (base + 1));
-        local = t - rank * (base + 1);
+    // which rank's slice holds gathered row t (T < 2^31: 32-bit arithmetic)
+    const uint32_t tu = (uint32_t)t, R = (uint32_t)a.R;
+    const uint32_t base = (uint32_t)a.T / R, extra = (uint32_t)a.T % R;
+    uint32_t rank, local;
+    if (tu < extra * (base + 1)) {
+        rank = tu / (base + 1);
+        local = tu - rank * (base + 1);
     } else {
-        const int64_t t2 = t - extra * (base + 1);
-        rank = (int)(extra + t2 / base);
+        const uint32_t t2 = tu - extra * (base + 1);
+        rank = extra + t2 / base;
         local = t2 - (rank - extra) * base;
     }
     const int hidden = a.hidden;
-    const uint16_t *row = a.inputs[rank] + local * hidden;
+    const uint16_t *row = a.inputs[rank] + (int64_t)local * hidden;
     const int nch = hidden >> 3, qc = a.q >> 3, kc = a.kv >> 3;
 
     uint4 v[CPL];
@@ -130,9 +131,9 @@ __global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_norm_kernel(const __gr
             for (int o = 8; o > 0; o >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
             if (is_x) {
-                const float sg = __fdiv_rn(amax, 448.0f);
+                const float sg = div_const_rn(amax, 448.0f, kRcp448);
                 if ((c & 15) == 0)
-                    st_f32(a.scale_out + t * (a.q >> 7) + (c >> 4), sg);
+                    st_f32_wb(a.scale_out + t * (a.q >> 7) + (c >> 4), sg);
                 st_v2(a.quant_out + t * a.q + (int64_t)c * 8,
                       sg != 0.0f ? e4m3_block_codes(nf, sg) : make_uint2(0, 0));
             }

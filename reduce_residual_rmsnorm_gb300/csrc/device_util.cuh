@@ -62,6 +62,14 @@ __device__ __forceinline__ void st_f32(void *p, float v)
     asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
+// Write-back store, for outputs so narrow per row that neighbouring rows share
+// a 32-byte sector (the all-gather's 1x128 block scales, 48 bytes per
+// 1536-wide x): the lines stay in L2 until the sector is complete.
+__device__ __forceinline__ void st_f32_wb(void *p, float v)
+{
+    asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // bf16 <-> fp32
 // ---------------------------------------------------------------------------
@@ -145,6 +153,22 @@ __device__ __forceinline__ float e4m3_value(uint32_t c)
                   : __int2float_rn((int)f) * 0.001953125f;  // 2^-9
     return (c & 0x80u) ? -mag : mag;
 }
+
+// RN(a / d) for a bf16-valued a >= 0 (a block's amax) and a constant divisor
+// d passed with its correctly rounded reciprocal r = RN(1/d), without a
+// divide: q0 = RN(a r), corrected once by the fused multiply-add remainder
+// RN(q0 d - a) (Markstein's correction, as below).  For d = 448 and d = 6 a
+// sweep of every non-negative bf16 value on the GPU checks it against the
+// IEEE divide bit for bit; an infinite or NaN a keeps q0 (inf or NaN, as the
+// divide).
+__device__ __forceinline__ float div_const_rn(float a, float d, float r)
+{
+    const float q0 = __fmul_rn(a, r);
+    const float q = __fmaf_rn(-__fmaf_rn(q0, d, -a), r, q0);
+    return a <= 0x1.fffffep127f ? q : q0;
+}
+constexpr float kRcp448 = 0x1.24924ap-9f;  // RN(1/448)
+constexpr float kRcp6 = 0x1.555556p-3f;    // RN(1/6)
 
 // E4M3 codes of the quotients n[i] / s of one FP8 1x128 block, s = amax/448
 // (amax the block's largest |n|, s > 0), for bf16-valued n, without a divide

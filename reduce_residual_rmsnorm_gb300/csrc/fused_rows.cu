@@ -209,7 +209,7 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1)
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float sg = __fdiv_rn(amax, 448.0f);
+            const float sg = div_const_rn(amax, 448.0f, kRcp448);
             if (live) {
                 if ((c & 15) == 0)
                     st_f32(static_cast<float *>(a.scale_out) + row * (a.H >> 7) + (c >> 4), sg);
@@ -221,7 +221,7 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
             for (int e = 0; e < 8; ++e)
                 amax = fmaxf(amax, fabsf(nf[e]));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // 16-element block
-            const uint32_t sf = cvt_e4m3(__fmul_rn(qscale, __fdiv_rn(amax, 6.0f)));
+            const uint32_t sf = cvt_e4m3(__fmul_rn(qscale, div_const_rn(amax, 6.0f, kRcp6)));
             const float d = e4m3_value(sf);
             uint32_t codes = 0;
             if (d != 0.0f) {

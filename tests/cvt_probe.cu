@@ -67,6 +67,24 @@ __global__ void block_codes_kernel(uint32_t *mismatch)
         atomicAdd(&mismatch[ab], bad);
 }
 
+// Every non-negative bf16 value a (bit patterns 0 .. 0x7FFF, +inf and NaNs
+// included): tsfn::div_const_rn for d = 448 (the 1x128 block scale) and d = 6
+// (the NVFP4 scale factor) against the IEEE quotients, bit for bit (NaN
+// against NaN).  mismatch[0] counts d = 448, mismatch[1] d = 6.
+__global__ void div_const_kernel(uint32_t *mismatch)
+{
+    const uint32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b > 0x7FFFu)
+        return;
+    const float a = __uint_as_float(b << 16);
+    const float g448 = tsfn::div_const_rn(a, 448.0f, tsfn::kRcp448), w448 = __fdiv_rn(a, 448.0f);
+    const float g6 = tsfn::div_const_rn(a, 6.0f, tsfn::kRcp6), w6 = __fdiv_rn(a, 6.0f);
+    if (!((isnan(g448) && isnan(w448)) || __float_as_uint(g448) == __float_as_uint(w448)))
+        atomicAdd(&mismatch[0], 1u);
+    if (!((isnan(g6) && isnan(w6)) || __float_as_uint(g6) == __float_as_uint(w6)))
+        atomicAdd(&mismatch[1], 1u);
+}
+
 }  // namespace
 
 extern "C" __attribute__((visibility("default"))) int cvt_probe(const float *x, int64_t n, uint16_t *bf16_out, uint8_t *e4m3_out, uint8_t *e2m1_out)
@@ -90,5 +108,12 @@ extern "C" __attribute__((visibility("default"))) int e4m3_values(float *out)
 extern "C" __attribute__((visibility("default"))) int block_codes_probe(uint32_t *mismatch)
 {
     block_codes_kernel<<<0x7F80, 256>>>(mismatch);
+    return (int)cudaGetLastError();
+}
+
+// mismatch: two counters, zeroed by the caller.
+extern "C" __attribute__((visibility("default"))) int div_const_probe(uint32_t *mismatch)
+{
+    div_const_kernel<<<128, 256>>>(mismatch);
     return (int)cudaGetLastError();
 }

@@ -6,7 +6,8 @@ midpoint of each format and its neighbours, zeros of both signs, subnormals,
 values past saturation and a million random fp32 bit patterns.  The FP8 1x128
 block quantiser's divide-free quotient gives the E4M3 code of the IEEE quotient
 over its whole domain (every positive bf16 amax up to +inf, every bf16 n with
-|n| <= amax)."""
+|n| <= amax), and the divide-free block scales amax / 448 and amax / 6 are the
+IEEE quotients for every non-negative bf16 amax."""
 import ctypes
 import os
 import subprocess
@@ -36,6 +37,8 @@ def probe(tmp_path_factory):
     lib.e4m3_values.restype = ctypes.c_int
     lib.block_codes_probe.argtypes = [ctypes.c_void_p]
     lib.block_codes_probe.restype = ctypes.c_int
+    lib.div_const_probe.argtypes = [ctypes.c_void_p]
+    lib.div_const_probe.restype = ctypes.c_int
     return lib
 
 
@@ -99,3 +102,10 @@ def test_block_quotient_codes_equal_the_ieee_divide_everywhere(probe):
     torch.cuda.synchronize()
     bad = mism.cpu().numpy()
     assert bad.sum() == 0, {hex(int(a)): int(bad[a]) for a in np.nonzero(bad)[0][:10]}
+
+
+def test_block_scale_quotients_equal_the_ieee_divide_everywhere(probe):
+    mism = torch.zeros(2, dtype=torch.int32, device="cuda:0")
+    assert probe.div_const_probe(mism.data_ptr()) == 0
+    torch.cuda.synchronize()
+    assert mism.cpu().tolist() == [0, 0]
