@@ -20,7 +20,13 @@
  * no inter-GPU synchronisation.
  *
  * Conventions for every entry point:
- *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *   - Every tensor pointer is device-accessible memory owned by the caller:
+ *     device memory, or page-locked host memory allocated or registered
+ *     through CUDA (cudaHostAlloc, cudaHostRegister), which on a system with
+ *     unified addressing a kernel reads and writes at its host address.  With
+ *     host buffers the kernel itself moves the bytes across the host link
+ *     (NVLink-C2C on a Grace-Blackwell node): no staging copy is needed.  A
+ *     pointer to ordinary pageable host memory is outside this contract.  The
  *     library allocates nothing, keeps no state between calls and never
  *     synchronises: a call validates its arguments on the host, enqueues one
  *     kernel on `stream` (a cudaStream_t; NULL = the legacy default stream)

@@ -1,6 +1,7 @@
 """ctypes binding of ``libts_fused_norm.so`` (include/ts_fused_norm.h).
 
-Argument marshalling only: tensors become device pointers, the stream is
+Argument marshalling only: tensors (CUDA, or pinned host tensors the kernels
+address across the host link) become pointers, the stream is
 PyTorch's current stream, and a non-zero status becomes a ``TsError``.  Every
 step of the computation runs in the library's CUDA kernels; there is no
 Python or CPU fallback, and calling without the built library raises.
@@ -154,11 +155,28 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def _dev(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor")
+    """A tensor the kernels can address: on the GPU, or in page-locked host
+    memory (read and written by the kernel across the host link)."""
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or (t.device.type == "cpu" and t.is_pinned())):
+        raise TypeError(f"{name} must be a CUDA tensor or a pinned host tensor")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     return t
+
+
+def _empty_like_place(shape, dtype, like: torch.Tensor) -> torch.Tensor:
+    """A new tensor where ``like`` lives: the same GPU, or pinned host memory."""
+    if like.is_cuda:
+        return torch.empty(shape, dtype=dtype, device=like.device)
+    return torch.empty(shape, dtype=dtype).pin_memory()
+
+
+def _scalar_like_place(value: float, like: torch.Tensor) -> torch.Tensor:
+    """One fp32 value where ``like`` lives, written before this returns (a
+    blocking host-to-device copy, or a pinned host tensor)."""
+    if like.is_cuda:
+        return torch.tensor([value], dtype=torch.float32, device=like.device)
+    return torch.tensor([value], dtype=torch.float32).pin_memory()
 
 
 def _rows(ts: torch.Tensor | Sequence[torch.Tensor], name: str) -> list[torch.Tensor]:
@@ -241,7 +259,7 @@ def ts_fused_reduce_norm(pattern: int, partials, residual: torch.Tensor | None =
             if not t.is_contiguous():
                 raise ValueError(f"{name} must be contiguous")
     if scale_factor is not None and not isinstance(scale_factor, torch.Tensor):
-        scale_factor = torch.tensor([float(scale_factor)], dtype=torch.float32, device=parts[0].device)
+        scale_factor = _scalar_like_place(float(scale_factor), parts[0])
     if scale_factor is not None:
         _dev(scale_factor, "scale_factor", torch.float32)
     outs = TsOuts(_ptr(allreduce_out), _ptr(residual_out), _ptr(norm_out), _ptr(partial_norm_out),
@@ -294,7 +312,7 @@ def ts_reducescatter_fused_norm(rs_pattern: int, partials, rank: int, add_in: to
             if not t.is_contiguous():
                 raise ValueError(f"{name} must be contiguous")
     if scale_factor is not None and not isinstance(scale_factor, torch.Tensor):
-        scale_factor = torch.tensor([float(scale_factor)], dtype=torch.float32, device=parts[0].device)
+        scale_factor = _scalar_like_place(float(scale_factor), parts[0])
     if scale_factor is not None:
         _dev(scale_factor, "scale_factor", torch.float32)
     outs = TsOuts(_ptr(reducescatter_out), _ptr(residual_out), _ptr(norm_out), None, 0, _ptr(quant_out),
@@ -361,9 +379,9 @@ def ts_qk_norm_sharded(shards, q_shard: int, k_shard: int, q_weight: torch.Tenso
     _dev(q_weight, "q_weight", torch.bfloat16)
     _dev(k_weight, "k_weight", torch.bfloat16)
     if q_out is None:
-        q_out = torch.empty((T, R * q_shard), dtype=torch.bfloat16, device=sh[0].device)
+        q_out = _empty_like_place((T, R * q_shard), torch.bfloat16, sh[0])
     if k_out is None:
-        k_out = torch.empty((T, R * k_shard), dtype=torch.bfloat16, device=sh[0].device)
+        k_out = _empty_like_place((T, R * k_shard), torch.bfloat16, sh[0])
     for name, t in (("q_out", q_out), ("k_out", k_out)):
         _dev(t, name, torch.bfloat16)
         if t.dim() != 2 or t.stride(1) != 1:
@@ -395,7 +413,7 @@ def ts_rms_norm_sharded(shards, width: int, weight: torch.Tensor, eps: float = 1
     R = len(sh)
     _dev(weight, "weight", torch.bfloat16)
     if out is None:
-        out = torch.empty((T, R * width), dtype=torch.bfloat16, device=sh[0].device)
+        out = _empty_like_place((T, R * width), torch.bfloat16, sh[0])
     _dev(out, "out", torch.bfloat16)
     if out.dim() != 2 or out.stride(1) != 1:
         raise ValueError("out must be 2-D with unit column stride")

@@ -253,12 +253,18 @@ def test_qk_rejects(lib, name, kw, want):
     assert detail
 
 
-def test_binding_requires_cuda_tensors():
+def test_binding_requires_cuda_or_pinned_tensors():
+    """Pageable host tensors are refused (only GPU and pinned host memory are
+    addressable by the kernels); pinned host tensors are accepted (on a GPU
+    box, tests/test_gpu_fused.py runs them)."""
     import torch
 
     x = torch.zeros(4, 64, dtype=torch.bfloat16)
-    with pytest.raises(TypeError):
+    assert not x.is_pinned()
+    with pytest.raises(TypeError, match="pinned host tensor"):
         pkg.ts_fused_reduce_norm(0, [x], allreduce_out=x)
+    with pytest.raises(TypeError):
+        pkg.ts_rms_norm_sharded([x], 64, x[0], 1e-6)
 
 
 def test_rms_zero_tokens_is_valid(lib):

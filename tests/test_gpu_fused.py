@@ -246,6 +246,40 @@ def test_in_place_allreduce_and_residual(dev):
     assert np.array_equal(host(parts2[0]), want["allreduce_out"])
 
 
+@pytest.mark.parametrize("pattern,layout", [(1, LIN), (3, SW128), (6, LIN)])
+def test_pinned_host_buffers(dev, pattern, layout):
+    """Inputs and outputs in pinned host memory (the kernel reads and writes
+    them across the host link): bit-identical to the same call on device
+    buffers."""
+    R, T, H = 4, 37, 2048
+    inp = _inputs(R, T, H, seed=13)
+    scale = 300.0 if pattern == 3 else None
+    want = _run_gpu(dev, pattern, inp, scale, 0, layout)
+    parts = [p.pin_memory() for p in inp["partials"]]
+    res, gamma = inp["residual"].pin_memory(), inp["gamma"].pin_memory()
+    outs = pkg.new_outputs(pattern, T, H, dev, sf_layout=layout, with_allreduce_out=True)
+    outs = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+    sf = None if scale is None else torch.tensor([scale], dtype=torch.float32).pin_memory()
+    pkg.ts_fused_reduce_norm(pattern, parts, res, gamma, EPS, sf, sf_layout=layout, **outs)
+    torch.cuda.synchronize()
+    assert set(outs) == set(want)
+    for k, v in outs.items():
+        assert np.array_equal(host(v).reshape(-1), want[k].reshape(-1)), k
+
+
+def test_pinned_host_buffers_sharded_norm(dev):
+    qs = wl.QKShape(R=8, T=21, q_shard=256, k_shard=64, v_shard=64)
+    qi = wl.qk_inputs(qs, seed=14)
+    q_d, k_d = pkg.ts_qk_norm_sharded(qi["shards"].to(dev), 256, 64, qi["q_weight"].to(dev), qi["k_weight"].to(dev),
+                                      EPS)
+    shards = [s.pin_memory() for s in qi["shards"]]
+    q_h, k_h = pkg.ts_qk_norm_sharded(shards, 256, 64, qi["q_weight"].pin_memory(), qi["k_weight"].pin_memory(),
+                                      EPS)
+    torch.cuda.synchronize()
+    assert q_h.device.type == "cpu" and q_h.is_pinned()
+    assert np.array_equal(wl.bits(q_h), wl.bits(q_d.cpu())) and np.array_equal(wl.bits(k_h), wl.bits(k_d.cpu()))
+
+
 def test_side_stream_and_zero_tokens(dev):
     inp = _inputs(2, 16, 4096, seed=9)
     s = torch.cuda.Stream()
