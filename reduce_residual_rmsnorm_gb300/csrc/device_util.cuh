@@ -70,6 +70,13 @@ __device__ __forceinline__ void st_f32_wb(void *p, float v)
     asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16, from a 16-byte aligned address) into L2
+// with one bulk request; nothing waits for it.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // bf16 <-> fp32
 // ---------------------------------------------------------------------------

@@ -45,6 +45,7 @@ struct FusedArgs {
     int sf_layout;      // kSfSwizzled128x4, kSfSwizzled8x4 or kSfLinear
     int64_t sf_rows;    // rows of the SF buffer (T, or T padded to 128 / 8)
     int64_t sf_cols;    // H/16, padded to a multiple of 4 when swizzled
+    int64_t prefetch_rows;  // rows ahead whose inputs a CTA prefetches into L2 (0: none)
 };
 
 struct QKArgs {
