@@ -65,6 +65,7 @@ struct QKArgs {
     int64_t ldq;
     uint16_t *k_out;
     int64_t ldk;
+    int64_t prefetch_tokens;  // tokens ahead whose shard rows a warp prefetches into L2 (0: none)
 };
 
 struct AGArgs {
