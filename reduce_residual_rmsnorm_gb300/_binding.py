@@ -143,7 +143,7 @@ def ts_status_string(status: int) -> str:
 
 
 def _ptr(t: torch.Tensor | None):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream) -> ctypes.c_void_p:
@@ -177,6 +177,29 @@ def _scalar_like_place(value: float, like: torch.Tensor) -> torch.Tensor:
     if like.is_cuda:
         return torch.tensor([value], dtype=torch.float32, device=like.device)
     return torch.tensor([value], dtype=torch.float32).pin_memory()
+
+
+def _partials(partials) -> tuple[list[int], int, int, torch.Tensor]:
+    """Pointers, T, H and one of the partials: R contiguous bf16 [T, H] tensors,
+    or one contiguous [R, T, H] tensor (whose rows are addressed without
+    making R views)."""
+    if isinstance(partials, torch.Tensor):
+        _dev(partials, "partials", torch.bfloat16)
+        if partials.dim() != 3:
+            raise ValueError("partials as one tensor must be [R, T, H]")
+        if partials.is_contiguous():
+            R, T, H = partials.shape
+            base, step = partials.data_ptr(), T * H * 2
+            return [base + r * step for r in range(R)], T, H, partials
+        partials = list(partials.unbind(0))
+    parts = [_dev(p, "partials[%d]" % i, torch.bfloat16) for i, p in enumerate(partials)]
+    if not parts:
+        raise ValueError("partials is empty")
+    T, H = parts[0].shape
+    for p in parts:
+        if p.shape != (T, H) or not p.is_contiguous():
+            raise ValueError("every partial must be a contiguous [T, H] tensor")
+    return [p.data_ptr() for p in parts], T, H, parts[0]
 
 
 def _rows(ts: torch.Tensor | Sequence[torch.Tensor], name: str) -> list[torch.Tensor]:
@@ -245,11 +268,7 @@ def ts_fused_reduce_norm(pattern: int, partials, residual: torch.Tensor | None =
     ``partial_norm_out``'s width gives partial_cols.
     ``launch_with_pdl``: programmatic dependent launch (TS_FLAG_PDL).
     """
-    parts = [_dev(p, "partials[%d]" % i, torch.bfloat16) for i, p in enumerate(_rows(partials, "partials"))]
-    T, H = parts[0].shape
-    for p in parts:
-        if p.shape != (T, H) or not p.is_contiguous():
-            raise ValueError("every partial must be a contiguous [T, H] tensor")
+    ptrs, T, H, part0 = _partials(partials)
     for name, t in (("residual", residual), ("gamma", gamma), ("allreduce_out", allreduce_out),
                     ("residual_out", residual_out), ("norm_out", norm_out),
                     ("partial_norm_out", partial_norm_out), ("quant_out", quant_out),
@@ -259,14 +278,14 @@ def ts_fused_reduce_norm(pattern: int, partials, residual: torch.Tensor | None =
             if not t.is_contiguous():
                 raise ValueError(f"{name} must be contiguous")
     if scale_factor is not None and not isinstance(scale_factor, torch.Tensor):
-        scale_factor = _scalar_like_place(float(scale_factor), parts[0])
+        scale_factor = _scalar_like_place(float(scale_factor), part0)
     if scale_factor is not None:
         _dev(scale_factor, "scale_factor", torch.float32)
     outs = TsOuts(_ptr(allreduce_out), _ptr(residual_out), _ptr(norm_out), _ptr(partial_norm_out),
                   0 if partial_norm_out is None else int(partial_norm_out.shape[-1]),
                   _ptr(quant_out), _ptr(scale_out), int(sf_layout), 0)
-    arr = (ctypes.c_void_p * len(parts))(*[p.data_ptr() for p in parts])
-    _check(library().ts_fused_reduce_norm(int(pattern), arr, len(parts), _ptr(residual), _ptr(gamma),
+    arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
+    _check(library().ts_fused_reduce_norm(int(pattern), arr, len(ptrs), _ptr(residual), _ptr(gamma),
                                           float(eps), _ptr(scale_factor), int(T), int(H),
                                           ctypes.byref(outs), TS_FLAG_PDL if launch_with_pdl else 0,
                                           _stream(stream)))
@@ -299,11 +318,7 @@ def ts_reducescatter_fused_norm(rs_pattern: int, partials, rank: int, add_in: to
     (``rs_token_split(T, R, rank)``); ``rank=-1`` computes every rank's slice
     in one launch (all T rows).
     """
-    parts = [_dev(p, "partials[%d]" % i, torch.bfloat16) for i, p in enumerate(_rows(partials, "partials"))]
-    T, H = parts[0].shape
-    for p in parts:
-        if p.shape != (T, H) or not p.is_contiguous():
-            raise ValueError("every partial must be a contiguous [T, H] tensor")
+    ptrs, T, H, part0 = _partials(partials)
     for name, t in (("add_in", add_in), ("residual", residual), ("gamma", gamma),
                     ("reducescatter_out", reducescatter_out), ("residual_out", residual_out),
                     ("norm_out", norm_out), ("quant_out", quant_out), ("scale_out", scale_out)):
@@ -312,13 +327,13 @@ def ts_reducescatter_fused_norm(rs_pattern: int, partials, rank: int, add_in: to
             if not t.is_contiguous():
                 raise ValueError(f"{name} must be contiguous")
     if scale_factor is not None and not isinstance(scale_factor, torch.Tensor):
-        scale_factor = _scalar_like_place(float(scale_factor), parts[0])
+        scale_factor = _scalar_like_place(float(scale_factor), part0)
     if scale_factor is not None:
         _dev(scale_factor, "scale_factor", torch.float32)
     outs = TsOuts(_ptr(reducescatter_out), _ptr(residual_out), _ptr(norm_out), None, 0, _ptr(quant_out),
                   _ptr(scale_out), int(sf_layout), 0)
-    arr = (ctypes.c_void_p * len(parts))(*[p.data_ptr() for p in parts])
-    _check(library().ts_reducescatter_fused_norm(int(rs_pattern), arr, len(parts), int(rank), _ptr(add_in),
+    arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
+    _check(library().ts_reducescatter_fused_norm(int(rs_pattern), arr, len(ptrs), int(rank), _ptr(add_in),
                                                  _ptr(residual), _ptr(gamma), float(eps), _ptr(scale_factor),
                                                  int(T), int(H), ctypes.byref(outs),
                                                  TS_FLAG_PDL if launch_with_pdl else 0, _stream(stream)))
