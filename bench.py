@@ -530,8 +530,9 @@ def _case_builders():
         shape = wl.WORKLOADS["C1"]
         inp = wl.fused_inputs(shape, seed=0, device=dev)
         outs = pkg.new_outputs(1, 16, 4096, dev)
-        call = lambda: pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS,  # noqa
-                                                stream=stream, **outs)
+        def call(pdl=False):
+            pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS, stream=stream,
+                                     launch_with_pdl=pdl, **outs)
         return call, fused_bytes(1, 2, 16, 4096)
 
     return {
@@ -575,9 +576,15 @@ def measure_rows(dev, stream, peak: float, iters: int) -> dict:
                     for _ in range(100):
                         call()
                 ms_graph = time_launches(graph.replay, 20, stream) / 100
-                rows[label] = {"us_stream_launch": ms_stream * 1e3, "us_in_cuda_graph": ms_graph * 1e3,
-                               "bytes": nbytes}
                 del graph
+                pdl_graph = torch.cuda.CUDAGraph()  # the same chain with launch_with_pdl
+                with torch.cuda.graph(pdl_graph, stream=stream):
+                    for _ in range(100):
+                        call(pdl=True)
+                ms_pdl = time_launches(pdl_graph.replay, 20, stream) / 100
+                del pdl_graph
+                rows[label] = {"us_stream_launch": ms_stream * 1e3, "us_in_cuda_graph": ms_graph * 1e3,
+                               "us_in_cuda_graph_pdl": ms_pdl * 1e3, "bytes": nbytes}
             else:
                 rows[label] = roofline_entry(nbytes, time_launches(call, iters, stream), peak)
         del call
