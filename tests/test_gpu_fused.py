@@ -322,6 +322,38 @@ def test_full_size_allreduce_rmsnorm(dev):
 
 
 @pytest.mark.slow
+def test_full_size_in_the_benchmark_configuration(dev):
+    """The headline step as bench.py times it: kARResidualRMSNorm R=8, T=4096,
+    H=7168, residual_out and norm_out only, launch_with_pdl, back-to-back
+    launches on a side stream; every row against the oracle.  Then the same
+    call on pinned host inputs and outputs (the end-to-end form): the same
+    bits as on device buffers."""
+    inp = wl.fused_inputs(wl.WORKLOADS["C2"], seed=0)
+    T, H = inp["residual"].shape
+    parts, res, gamma = inp["partials"].to(dev), inp["residual"].to(dev), inp["gamma"].to(dev)
+    ro = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    no = torch.empty_like(ro)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(5):
+            pkg.ts_fused_reduce_norm(1, parts, res, gamma, EPS, residual_out=ro, norm_out=no,
+                                     launch_with_pdl=True, stream=s)
+    torch.cuda.synchronize()
+    got = {"residual_out": host(ro), "norm_out": host(no)}
+    want = _oracle(1, inp)
+    assert np.array_equal(got["residual_out"], want["residual_out"])
+    assert_bf16_close(got["norm_out"], want["norm_out"], 1, 0.999, "norm_out")
+
+    h_ro = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    h_no = torch.empty_like(h_ro).pin_memory()
+    pkg.ts_fused_reduce_norm(1, inp["partials"].pin_memory(), inp["residual"].pin_memory(),
+                             inp["gamma"].pin_memory(), EPS, residual_out=h_ro, norm_out=h_no,
+                             launch_with_pdl=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(h_ro), got["residual_out"]) and np.array_equal(host(h_no), got["norm_out"])
+
+
+@pytest.mark.slow
 def test_full_size_fp8(dev):
     """FP8 per-tensor, FP8 1x128 blockwise, PartialOut (+FP8 blockwise), R=8,
     T=8192, H=7168 with 0.1 % outliers x50."""
