@@ -42,6 +42,10 @@
  *   c13 two E2M1 codes per byte, even element in the low nibble.
  *   c14 SWIZZLED_128x4 scale-factor tile map (see orc_sf_offset_swizzled_128x4).
  *   c21 SWIZZLED_8x4 scale-factor tile map (see orc_sf_offset_swizzled_8x4).
+ *       Parity unpinned: the pages only name these two layouts, so both maps
+ *       are readings; the tests pin what follows from the readings (each map
+ *       is a bijection onto the padded buffer with the stated tile structure
+ *       and zero padding), not the layouts themselves.
  *   c15 partial_norm_out holds the first P columns of n; the RMS is over all H.
  *   c18 QK: rsqrt(V / R + eps), V the fp32 shard-ascending sum of shard means.
  *   c25 a sum of squares past fp32's range is +inf (fp32 accumulation), so
