@@ -42,10 +42,12 @@
  *   c13 two E2M1 codes per byte, even element in the low nibble.
  *   c14 SWIZZLED_128x4 scale-factor tile map (see orc_sf_offset_swizzled_128x4).
  *   c21 SWIZZLED_8x4 scale-factor tile map (see orc_sf_offset_swizzled_8x4).
- *       Parity unpinned: the pages only name these two layouts, so both maps
- *       are readings; the tests pin what follows from the readings (each map
- *       is a bijection onto the padded buffer with the stated tile structure
- *       and zero padding), not the layouts themselves.
+ *       The pages only name these two layouts, so both maps are readings.
+ *       The 128x4 map is pinned to the layout an NVFP4 block-scaled GEMM
+ *       reads its scales in (a GPU test feeds scales placed by this map to
+ *       PyTorch's NVFP4 scaled matmul).  The 8x4 map is parity unpinned: the
+ *       tests pin only what follows from the reading (a bijection onto the
+ *       padded buffer, the tile structure, zero padding).
  *   c15 partial_norm_out holds the first P columns of n; the RMS is over all H.
  *   c18 QK: rsqrt(V / R + eps), V the fp32 shard-ascending sum of shard means.
  *   c25 a sum of squares past fp32's range is +inf (fp32 accumulation), so
