@@ -63,7 +63,7 @@ typedef enum {
     TS_ERR_NULL = -2,        /* a required pointer is NULL                              */
     TS_ERR_SHAPE = -3,       /* sizes out of range / not multiples the pattern requires  */
     TS_ERR_ALIGN = -4,       /* a pointer is not aligned as required                     */
-    TS_ERR_UNSUPPORTED = -5, /* valid request this build does not implement, or an output
+    TS_ERR_UNSUPPORTED = -5, /* valid request the library does not implement, or an output
                                 pointer the pattern does not define                      */
     TS_ERR_ALIAS = -6,       /* overlapping buffers (other than the allowed in-place ones) */
     TS_ERR_LAUNCH = -7       /* the CUDA launch failed                                    */
