@@ -166,15 +166,15 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     if constexpr (EP == Epilogue::kAllReduce)
         return;
 
-    // ---- row reduction of x^2 (same order in every thread) -----------------
+    // ---- row reduction of x^2 (the same bits in every thread) --------------
     __shared__ float red[kMaxThreads / 32];
     ss = warp_sum(ss);
     if (lane == 0)
         red[tid >> 5] = ss;
     __syncthreads();
-    float tot = 0.0f;
-    for (int w = 0; w < (nthr >> 5); ++w)
-        tot += red[w];
+    // every warp folds the per-warp sums with the same butterfly, so every
+    // thread gets the same bits (each step adds the same two values)
+    const float tot = warp_sum(lane < (nthr >> 5) ? red[lane] : 0.0f);
     const float scale = rsqrtf(__fadd_rn(__fdiv_rn(tot, (float)a.H), a.eps));
 
     float qscale = 0.0f;
