@@ -335,6 +335,10 @@ cudaError_t launch_rb(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t s)
 
 cudaError_t launch_fused(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t stream)
 {
+    // the partial loop is unrolled to RB with a predicate per partial, so the
+    // small R of tensor parallelism 1 and 2 get their own instances
+    if (a.R == 1) return launch_rb<1>(ep, a, pdl, stream);
+    if (a.R == 2) return launch_rb<2>(ep, a, pdl, stream);
     if (a.R <= 4) return launch_rb<4>(ep, a, pdl, stream);
     if (a.R <= 8) return launch_rb<8>(ep, a, pdl, stream);
     return launch_rb<16>(ep, a, pdl, stream);
