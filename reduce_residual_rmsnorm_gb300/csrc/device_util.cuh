@@ -120,13 +120,24 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
     return r;
 }
 
+// Four fp32 -> four E4M3 codes in one word, element i in byte i (the two
+// 16-bit pairs packed by one move).
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float f0, float f1, float f2, float f3)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(f0), "f"(f1), "f"(f2), "f"(f3));
+    return r;
+}
+
 // Eight fp32 -> eight E4M3 codes, element i in byte i.
 __device__ __forceinline__ uint2 cvt_e4m3x8(const float (&f)[8])
 {
-    uint2 r;
-    r.x = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
-    r.y = cvt_e4m3x2(f[4], f[5]) | (cvt_e4m3x2(f[6], f[7]) << 16);
-    return r;
+    return make_uint2(cvt_e4m3x4(f[0], f[1], f[2], f[3]), cvt_e4m3x4(f[4], f[5], f[6], f[7]));
 }
 
 // Two fp32 -> two E2M1 codes (nearest-even, saturating to +-6); lo in bits 0..3.
@@ -141,11 +152,20 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi)
     return r;
 }
 
-// Eight fp32 -> eight E2M1 codes packed in 32 bits, element i in nibble i.
+// Eight fp32 -> eight E2M1 codes packed in 32 bits, element i in nibble i
+// (four byte-sized pairs packed by one move).
 __device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&f)[8])
 {
-    return cvt_e2m1x2(f[0], f[1]) | (cvt_e2m1x2(f[2], f[3]) << 8) |
-           (cvt_e2m1x2(f[4], f[5]) << 16) | (cvt_e2m1x2(f[6], f[7]) << 24);
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]));
+    return r;
 }
 
 // One fp32 -> one E4M3 code.
