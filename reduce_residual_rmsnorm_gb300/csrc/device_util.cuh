@@ -172,13 +172,19 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&f)[8])
 __device__ __forceinline__ uint32_t cvt_e4m3(float v) { return cvt_e4m3x2(v, 0.0f) & 0xFFu; }
 
 // Value of an E4M3 code (FN variant: bias 7; exponent field 0 is subnormal,
-// f * 2^-9).  Codes 0x7F/0xFF (NaN) never come out of a saturating cvt.
+// f * 2^-9; 0x7F / 0xFF are NaN), by the hardware conversion to f16 (which
+// holds every E4M3 value exactly) and from f16 to fp32.
 __device__ __forceinline__ float e4m3_value(uint32_t c)
 {
-    const uint32_t e = (c >> 3) & 0xFu, f = c & 0x7u;
-    float mag = e ? __uint_as_float(((e + 120u) << 23) | (f << 20))
-                  : __int2float_rn((int)f) * 0.001953125f;  // 2^-9
-    return (c & 0x80u) ? -mag : mag;
+    float v;
+    asm("{\n\t.reg .b16 h, lo, hi;\n\t.reg .b32 d;\n\t"
+        "cvt.u16.u32 h, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 d, h;\n\t"
+        "mov.b32 {lo, hi}, d;\n\t"
+        "cvt.f32.f16 %0, lo;\n\t}"
+        : "=f"(v)
+        : "r"(c & 0xFFu));
+    return v;
 }
 
 // RN(a / d) for a bf16-valued a >= 0 (a block's amax) and a constant divisor

@@ -92,8 +92,9 @@ def test_e4m3_decoder_matches_the_oracle(probe):
     torch.cuda.synchronize()
     got = out.cpu().numpy()
     want = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
-    fin = np.isfinite(want)  # 0x7F / 0xFF are NaN codes, never produced by a saturating cvt
+    fin = np.isfinite(want)  # 0x7F / 0xFF are the NaN codes
     assert np.array_equal(got[fin].view(np.uint32), want[fin].view(np.uint32))
+    assert np.isnan(got[~fin]).all()
 
 
 def test_block_quotient_codes_equal_the_ieee_divide_everywhere(probe):
