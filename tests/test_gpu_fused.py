@@ -152,6 +152,8 @@ SHAPES = [  # (R, T, H)
     (5, 130, 5120),
     (4, 3, 16384),
     (7, 64, 2112),
+    (1, 1300, 1024),  # R = 1 instance; T beyond one wave, so the L2 prefetch runs
+    (2, 700, 2048),   # R = 2 instance, likewise
 ]
 
 
