@@ -60,6 +60,7 @@ CASES = [  # R, T, Q, K, V, ldq pad, ldk pad
     (16, 5, 384, 64, 64, 0, 0),
     (8, 3, 4096, 1024, 8, 64, 64),
     (5, 130, 256, 512, 0, 0, 0),
+    (2, 6000, 256, 64, 16, 0, 0),    # two tokens per warp; T beyond one wave, so the L2 prefetch runs
 ]
 
 
@@ -121,7 +122,7 @@ def _rms_inputs(R, T, W, extra, seed):
 
 
 RMS_CASES = [(8, 33, 768, 0, 0), (1, 1, 8, 0, 0), (2, 9, 3072, 0, 0), (3, 17, 136, 24, 8),
-             (16, 5, 384, 64, 0), (5, 130, 4096, 8, 16), (4, 64, 1024, 0, 64)]
+             (16, 5, 384, 64, 0), (5, 130, 4096, 8, 16), (4, 64, 1024, 0, 64), (8, 3000, 768, 0, 0)]
 
 
 @pytest.mark.parametrize("R,T,W,extra,pad", RMS_CASES, ids=[f"R{c[0]}-T{c[1]}-W{c[2]}" for c in RMS_CASES])
