@@ -19,8 +19,10 @@ beside it), the CPU
 oracle timed on a bounded sample of rows, the SM clocks sampled during the
 timed region, and ``rows``: the other patterns and workloads timed the same
 way (kAllReduce; FP8 per-tensor, FP8 1x128 blockwise, PartialOut on R=8,
-T=8192; NVFP4 on R=4, T=16384, H=5120 in both SF layouts; the sharded
-MiniMax QK-norm on R=8, T=32768; and the R=2, T=16 latency case).
+T=8192; NVFP4 on R=4, T=16384, H=5120 in the three SF layouts; tensor-parallel
+degrees 1, 2 and 4 on T=16384, H=5120; the reduce-scatter and all-gather forms;
+the sharded MiniMax QK-norm and single-matrix norm on R=8, T=32768; and the R=2,
+T=16 latency case).
 
 ``--impl reference`` times the CPU oracle instead (host cores, bounded samples
 of the same workload per step); under torchrun only rank 0 runs it.
@@ -535,6 +537,24 @@ def _case_builders():
                                      launch_with_pdl=pdl, **outs)
         return call, fused_bytes(1, 2, 16, 4096)
 
+    def tp(pattern, R):
+        """Smaller tensor-parallel degrees on the R=4 T=16384 H=5120 shape."""
+        def build(dev, stream):
+            T, H = 16384, 5120
+            inp = wl.fused_inputs(wl.FusedShape(R=R, T=T, H=H), seed=0, device=dev)
+            g = None
+            if pattern in (2, 3):
+                norm = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+                pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS,
+                                         residual_out=torch.empty_like(norm), norm_out=norm, stream=stream)
+                g = ((2688.0 if pattern == 3 else 448.0) / norm.float().abs().max()).reshape(1).to(torch.float32)
+                del norm
+            outs = pkg.new_outputs(pattern, T, H, dev)
+            call = lambda: pkg.ts_fused_reduce_norm(pattern, inp["partials"], inp["residual"],  # noqa: E731
+                                                    inp["gamma"], EPS, g, stream=stream, **outs)
+            return call, fused_bytes(pattern, R, T, H)
+        return build
+
     return {
         "c2-p1": ("kARResidualRMSNorm R=8 T=4096 H=7168 launch_with_pdl", c2(1, True)),
         "c2-p1-nopdl": ("kARResidualRMSNorm R=8 T=4096 H=7168 (plain launch)", c2(1)),
@@ -554,6 +574,11 @@ def _case_builders():
         "ag-rms-fp8b": ("kAllGatherfusedRMSFP8BlockWiseQuant R=8 T=65536 1536|512|64", ag(2)),
         "c5-qk": ("MiniMax QK-RMSNorm R=8 T=32768 Q=1024 K=128", c5),
         "single-768": ("single-matrix sharded RMSNorm R=8 T=32768 W=768", single),
+        "tp1-p1": ("kARResidualRMSNorm R=1 T=16384 H=5120", tp(1, 1)),
+        "tp2-p1": ("kARResidualRMSNorm R=2 T=16384 H=5120", tp(1, 2)),
+        "tp2-p3": ("kARResidualRMSNormFP4Quant R=2 T=16384 H=5120 SF LINEAR", tp(3, 2)),
+        "tp2-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=2 T=16384 H=5120", tp(6, 2)),
+        "tp4-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=4 T=16384 H=5120", tp(6, 4)),
         "c1-p1": ("kARResidualRMSNorm R=2 T=16 H=4096 (latency)", c1),
     }
 
