@@ -199,6 +199,21 @@ def test_zero_rows(dev):
             assert (v == 0).all(), (pattern, k)
 
 
+def test_negative_zero_partials_reduce_to_positive_zero(dev):
+    """Reading c1: the sum starts from a +0 accumulator, so partials that are
+    all -0 reduce to +0 (bit pattern 0x0000), and so does x with a -0
+    residual; the norm of such a row is +0 times gamma."""
+    R, T, H = 3, 4, 256
+    negz = torch.full((R, T, H), -0.0, dtype=torch.bfloat16)
+    inp = {"partials": negz, "residual": torch.full((T, H), -0.0, dtype=torch.bfloat16),
+           "gamma": torch.ones(H, dtype=torch.bfloat16)}
+    got = _run_gpu(dev, 1, inp, allreduce=True)
+    want = _oracle(1, inp)
+    for k in ("allreduce_out", "residual_out", "norm_out"):
+        assert np.array_equal(got[k], want[k]), k
+        assert (got[k] == 0).all(), k
+
+
 def test_saturation_and_extremes(dev):
     R, T, H = 4, 8, 512
     inp = _inputs(R, T, H, seed=7, p_std=3.0e4)  # large values: x^2 ~ 1e10 per element
