@@ -76,12 +76,7 @@ __global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_norm_kernel(const __gr
     for (int i = 0; i < CPL; ++i) {
         const int c = lane + 32 * i;
         if (c < qc + kc) {
-            float f[8];
-            unpack8(v[i], f);
-            float s = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                s = fmaf(f[e], f[e], s);
+            const float s = sumsq_bf16x8(v[i], 0.0f);
             if (c < qc)
                 sx += s;
             else

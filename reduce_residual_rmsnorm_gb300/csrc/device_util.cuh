@@ -94,6 +94,38 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
     f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
+// acc[i] = RN(acc[i] + element i of the 8 bf16 in v): Blackwell's mixed
+// bf16 + fp32 add widens the bf16 operand exactly inside the instruction, so
+// this is bit for bit __fadd_rn(acc[i], widened element i) without unpacking.
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &v)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("{\n\t.reg .b16 lo, hi;\n\t"
+            "mov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.bf16 %0, lo, %0;\n\t"
+            "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+            : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1])
+            : "r"(w[i]));
+}
+
+// s = RN(e * e + s) over the 8 bf16 elements of v in order, each product of
+// the exactly widened element with itself (the mixed bf16 fma).
+__device__ __forceinline__ float sumsq_bf16x8(const uint4 &v, float s)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("{\n\t.reg .b16 lo, hi;\n\t"
+            "mov.b32 {lo, hi}, %1;\n\t"
+            "fma.rn.f32.bf16 %0, lo, lo, %0;\n\t"
+            "fma.rn.f32.bf16 %0, hi, hi, %0;\n\t}"
+            : "+f"(s)
+            : "r"(w[i]));
+    return s;
+}
+
 // Round two fp32 values to bf16 (nearest, ties to even); lo in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {

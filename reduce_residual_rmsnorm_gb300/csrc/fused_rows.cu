@@ -128,29 +128,18 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
                 for (int e = 0; e < 8; ++e)
                     acc[e] = 0.0f;
 #pragma unroll
-                for (int r = 0; r < RB; ++r) {
-                    if (r < a.R) {
-                        float f[8];
-                        unpack8(raw[u][r], f);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            acc[e] = __fadd_rn(acc[e], f[e]);
-                    }
-                }
+                for (int r = 0; r < RB; ++r)
+                    if (r < a.R)
+                        add_bf16x8(acc, raw[u][r]);
                 if (EP == Epilogue::kAllReduce || a.allreduce_out != nullptr)
                     st_v4(a.allreduce_out + off, pack8(acc));
                 if constexpr (EP != Epilogue::kAllReduce) {
-                    float f[8];
-                    if constexpr (ADD) {  // x = ((sum) + add_in) + residual
-                        unpack8(addv[u], f);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            acc[e] = __fadd_rn(acc[e], f[e]);
-                    }
-                    unpack8(res[u], f);
+                    if constexpr (ADD)  // x = ((sum) + add_in) + residual
+                        add_bf16x8(acc, addv[u]);
+                    add_bf16x8(acc, res[u]);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        x[v][e] = __fadd_rn(acc[e], f[e]);
+                        x[v][e] = acc[e];
                         ss = fmaf(x[v][e], x[v][e], ss);
                     }
                     st_v4(a.residual_out + off, pack8(x[v]));

@@ -88,24 +88,14 @@ __global__ void __launch_bounds__(kMaxThreads) qk_norm_kernel(const __grid_const
 #pragma unroll
         for (int i = 0; i < QC; ++i) {
             const int c = lane + 32 * i;
-            if (live && c < qn) {
-                float f[8];
-                unpack8(qv[j][i], f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    sq[j] = fmaf(f[e], f[e], sq[j]);
-            }
+            if (live && c < qn)
+                sq[j] = sumsq_bf16x8(qv[j][i], sq[j]);
         }
 #pragma unroll
         for (int i = 0; i < KC; ++i) {
             const int c = lane + 32 * i;
-            if (live && c < kn) {
-                float f[8];
-                unpack8(kv[j][i], f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    sk[j] = fmaf(f[e], f[e], sk[j]);
-            }
+            if (live && c < kn)
+                sk[j] = sumsq_bf16x8(kv[j][i], sk[j]);
         }
     }
     pdl_launch_dependents();
