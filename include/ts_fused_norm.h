@@ -170,15 +170,16 @@ typedef struct {
  *   then the outputs listed above for the pattern.
  *
  *   pattern       ts_pattern_t.
- *   partials      host array of R device pointers, each bf16 [T, H].
+ *   partials      host array of R device-accessible pointers, each bf16 [T, H].
  *   R             1..16.
  *   residual      bf16 [T, H]; required for patterns 1..8 (ignored for 0).
  *   gamma         bf16 [H] (rms_gamma); required for patterns 1..8.
  *   eps           rms_eps, added inside the rsqrt (e.g. 1e-6).
- *   scale_factor  device fp32[1]: the per-tensor FP8 scale sigma (patterns 2, 4:
- *                 code = e4m3(n * sigma)) or the NVFP4 global scale g (patterns
- *                 3, 5); required for 2..5, ignored otherwise.  A device pointer
- *                 so the call can be captured in a CUDA graph.
+ *   scale_factor  fp32[1] in device-accessible memory: the per-tensor FP8 scale
+ *                 sigma (patterns 2, 4: code = e4m3(n * sigma)) or the NVFP4
+ *                 global scale g (patterns 3, 5); required for 2..5, ignored
+ *                 otherwise.  A pointer, read by the kernel, so the call can be
+ *                 captured in a CUDA graph.
  *   T             rows (tokens), >= 0.  T == 0 validates and returns TS_OK
  *                 without launching; the per-row buffers (partials, residual,
  *                 outputs) may then be NULL, as empty tensors are.
@@ -221,7 +222,7 @@ typedef enum {
  *
  *   rs_pattern    ts_rs_pattern_t.  0..6 behave as AllReduceFusionPattern
  *                 0..6 on the slice; 7 = 6 with add_in; 8 = 1 with add_in.
- *   partials      host array of R device pointers, each bf16 [T, H] (all T
+ *   partials      host array of R device-accessible pointers, each bf16 [T, H] (all T
  *                 tokens; only the slice's rows are read).
  *   rank          0..R-1, or -1 for every rank's slice in one launch (the
  *                 slices in rank order are all T tokens: count = T, start = 0).
@@ -259,7 +260,7 @@ typedef enum {
  *   The rope columns only appear in allgather_out.
  *
  *   ag_pattern    ts_ag_pattern_t.
- *   inputs        host array of R device pointers; inputs[r] is bf16
+ *   inputs        host array of R device-accessible pointers; inputs[r] is bf16
  *                 [count_r, hidden] (may be NULL when count_r == 0).
  *   T             gathered tokens, >= 0 (T == 0 returns TS_OK).
  *   hidden        = q_lora_rank + kv_lora_rank + qk_rope_head_dim <= 2112.
@@ -291,7 +292,7 @@ TS_API int ts_allgather_fused_norm(int ag_pattern, const void *const *inputs, in
  *   q_out[t, r*Q + j] = bf16((x_r[t,j]   * rsqrt(Vq[t]/R + eps)) * q_weight[r*Q + j])
  *   k_out[t, r*K + j] = bf16((x_r[t,Q+j] * rsqrt(Vk[t]/R + eps)) * k_weight[r*K + j])
  *
- *   qkv_shards    host array of R device pointers; shard r is bf16 [T, row_stride]
+ *   qkv_shards    host array of R device-accessible pointers; shard r is bf16 [T, row_stride]
  *                 holding q (Q columns) | k (K columns) | v (not read).
  *   R             1..16.
  *   T             tokens, >= 0 (T == 0 returns TS_OK without launching; the
@@ -324,7 +325,7 @@ TS_API int ts_qk_norm_sharded(const void *const *qkv_shards, int R, int64_t T, i
  *   V[t]   = sum over r ascending of v_r[t]                             fp32
  *   out[t, r*W + j] = bf16((x_r[t,j] * rsqrt(V[t]/R + eps)) * weight[r*W + j])
  *
- *   shards        host array of R device pointers, shard r bf16 [T, row_stride]
+ *   shards        host array of R device-accessible pointers, shard r bf16 [T, row_stride]
  *                 (its slice in the first W columns).
  *   R             1..16.     T: tokens, >= 0 (T == 0 returns TS_OK).
  *   row_stride    multiple of 8, >= W.
