@@ -61,6 +61,8 @@ CASES = [  # R, T, Q, K, V, ldq pad, ldk pad
     (8, 3, 4096, 1024, 8, 64, 64),
     (5, 130, 256, 512, 0, 0, 0),
     (2, 6000, 256, 64, 16, 0, 0),    # two tokens per warp; T beyond one wave, so the L2 prefetch runs
+    (3, 40, 512, 512, 64, 8, 0),      # 2 + 2 chunks per lane: weights loaded before the barrier
+    (2, 21, 256, 1024, 0, 0, 8),      # 1 + 4 chunks per lane, likewise
 ]
 
 
