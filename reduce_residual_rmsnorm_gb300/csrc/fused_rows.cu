@@ -77,7 +77,8 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     // quantises or R = 1 (NVFP4 R=4 T=16384 H=5120: 153.1 us against 157.4;
     // kARResidualRMSNorm R=1 T=16384 H=7168: 136.7 against 155.7), losses of
     // about 2 % for the bf16 patterns at R = 2..4 and for every R = 8 pattern,
-    // which therefore do not prefetch.
+    // which therefore do not prefetch.  For R > 1 the launch enables it only
+    // from 3.5 R waves of rows on (launch_rb).
     if constexpr (RB <= 4) {
         constexpr bool kQuant = EP == Epilogue::kFp8Tensor || EP == Epilogue::kFp4 || EP == Epilogue::kFp8Block;
         if ((kQuant || a.R == 1) && tid < 32 && a.prefetch_rows > 0 && row + a.prefetch_rows < a.T) {
@@ -332,7 +333,15 @@ cudaError_t launch_rb(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t s)
             const int cap = V <= 2 ? reg_cap<RB, 2>() : reg_cap<RB, 4>();
             int per_sm = 65536 / (nthr * cap);
             per_sm = per_sm < 2048 / nthr ? per_sm : 2048 / nthr;
-            b.prefetch_rows = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+            const int64_t wave = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+            // The first wave's loads queue behind the prefetches of the second
+            // wave's R+1 rows, a start-up cost that only enough waves repay.
+            // Measured crossovers: R = 1 gains from 9 waves on (H=7168 T=2736:
+            // 25.5 us against 28.8); R = 2 is even at 9 waves and gains from 12;
+            // R = 4 loses up to 12 waves (NVFP4 H=5120 T=4560: 47.7 against
+            // 42.6) and gains from 14.  Hence from 3.5 R waves on, for R > 1.
+            if (a.R == 1 || 2 * a.T >= 7 * (int64_t)a.R * wave)
+                b.prefetch_rows = wave;
         }
     }
     if (V == 1) return launch_rb_v<RB, 1>(ep, b, nthr, grid, pdl, s);

@@ -153,7 +153,7 @@ SHAPES = [  # (R, T, H)
     (4, 3, 16384),
     (7, 64, 2112),
     (1, 1300, 1024),  # R = 1 instance; T beyond one wave, so the L2 prefetch runs
-    (2, 700, 2048),   # R = 2 instance, likewise
+    (2, 4300, 2048),  # R = 2 instance past 3.5 R waves of CTAs, so the L2 prefetch runs too
     (16, 5, 16384),   # the widest row with the most partials: 4 chunks per thread
     (8, 4, 16256),    # 4 chunks per thread with a ragged last chunk set (2032 of 2048)
 ]
