@@ -26,6 +26,8 @@ T=16 latency case).
 
 ``--impl reference`` times the CPU oracle instead (host cores, bounded samples
 of the same workload per step); under torchrun only rank 0 runs it.
+``--sweep-t`` prints only the per-call time of single fused calls against T,
+with the inputs cold in L2 (one JSON line per shape and T).
 """
 from __future__ import annotations
 
@@ -638,6 +640,70 @@ def profile_case(key: str, launches: int) -> None:
     print(json.dumps({"case": key, "label": label, "launches": launches, "bytes_per_launch": nbytes}))
 
 
+# (pattern, R, H) and T values of the per-call table: single calls with the inputs cold in L2
+SWEEP_SHAPES = ((1, 8, 7168), (6, 8, 7168), (3, 4, 5120), (1, 2, 4096))
+SWEEP_TOKENS = (1, 16, 64, 256, 1024, 4096, 16384)
+
+
+def sweep_t(reps: int = 40) -> None:
+    """Per-call time of single fused calls (launch_with_pdl) against T, with the
+    inputs cold in L2: a CUDA graph of ``reps`` x (read a 256 MB buffer, call),
+    minus a graph of ``reps`` reads alone.  One JSON line per (shape, T)."""
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import reduce_residual_rmsnorm_gb300 as pkg
+    from reduce_residual_rmsnorm_gb300 import workloads as wl
+
+    peak, peak_kind = read_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    acc = torch.zeros(1, dtype=torch.float32, device=dev)
+
+    def read_flush():
+        torch.sum(flush, dim=0, keepdim=True, out=acc)
+
+    def graph_of(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(reps):
+                    fn()
+        return g
+
+    def per_call_ms(g):
+        with torch.cuda.stream(stream):
+            return min(time_launches(g.replay, 5, stream) for _ in range(3)) / reps
+
+    g_flush = graph_of(read_flush)
+    print(json.dumps({"flush_us": per_call_ms(g_flush) * 1e3}), flush=True)
+    for p, R, H in SWEEP_SHAPES:
+        for T in SWEEP_TOKENS:
+            inp = wl.fused_inputs(wl.FusedShape(R=R, T=T, H=H), seed=0, device=dev)
+            outs = pkg.new_outputs(p, T, H, dev)
+            sf = torch.tensor([100.0], device=dev) if p in (2, 3, 4, 5) else None
+
+            def both():
+                read_flush()
+                pkg.ts_fused_reduce_norm(p, inp["partials"], inp["residual"], inp["gamma"], EPS, sf,
+                                         stream=stream, launch_with_pdl=True, **outs)
+
+            g = graph_of(both)
+            ms = per_call_ms(g) - per_call_ms(g_flush)
+            nb = fused_bytes(p, R, T, H)
+            print(json.dumps({"pattern": p, "R": R, "T": T, "H": H, "us": ms * 1e3,
+                              "frac": nb / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind}), flush=True)
+            del g, inp, outs
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -786,10 +852,14 @@ def main(argv=None):
     ap.add_argument("--profile-case", default=None,
                     help="only set up this named workload and launch it --launches times (for ncu)")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--sweep-t", action="store_true",
+                    help="only print the per-call time of single cold fused calls against T")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.profile_case:
+    if args.sweep_t:
+        sweep_t()
+    elif args.profile_case:
         profile_case(args.profile_case, args.launches)
     elif args.impl == "reference":
         run_reference(args)
