@@ -156,6 +156,8 @@ SHAPES = [  # (R, T, H)
     (2, 4300, 2048),  # R = 2 instance past 3.5 R waves of CTAs, so the L2 prefetch runs too
     (16, 5, 16384),   # the widest row with the most partials: 4 chunks per thread
     (8, 4, 16256),    # 4 chunks per thread with a ragged last chunk set (2032 of 2048)
+    (3, 37, 1040),    # 65 NVFP4 scale factors per row: byte stores, swizzled padding columns
+    (2, 130, 4112),   # 257 per row, 2 chunks per thread, ragged
 ]
 
 
