@@ -464,7 +464,8 @@ def test_pdl_dependent_chain_matches_plain(dev):
 # reduce-scatter fusion restated for one GPU (every rank's slice)
 # ---------------------------------------------------------------------------
 
-RS_SHAPES = [(4, 37, 1024), (8, 64, 7168), (3, 2, 256), (2, 16, 4096)]
+RS_SHAPES = [(4, 37, 1024), (8, 64, 7168), (3, 2, 256), (2, 16, 4096),
+             (1, 1300, 1024)]  # R = 1 beyond one wave of CTAs: the L2 prefetch of add_in runs
 
 
 @pytest.mark.parametrize("R,T,H", RS_SHAPES, ids=[f"R{r}-T{t}-H{h}" for r, t, h in RS_SHAPES])
@@ -543,9 +544,11 @@ def test_sum_of_squares_overflow(dev):
             assert (got["norm_out"][0] == 0x0000).all() and (got["norm_out"][1] == 0x8000).all()
 
 
-def test_reducescatter_all_ranks_in_one_launch(dev):
-    """rank = -1: every rank's slice in one launch equals the per-rank calls."""
-    R, T, H = 8, 1000, 7168
+@pytest.mark.parametrize("R,T,H", [(8, 1000, 7168), (2, 8600, 1024)])
+def test_reducescatter_all_ranks_in_one_launch(dev, R, T, H):
+    """rank = -1: every rank's slice in one launch equals the per-rank calls
+    (with R = 2 over 8600 rows the one launch prefetches into L2, the per-rank
+    calls of 4300 rows do not)."""
     inp = _inputs(R, T, H, seed=13)
     g = torch.Generator().manual_seed(5)
     add = torch.randn((T, H), generator=g).to(torch.bfloat16).to(dev)
