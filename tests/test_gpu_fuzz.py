@@ -1,10 +1,13 @@
 """Seeded random configurations of every entry point against the oracle.
 
-40 draws of (entry point, pattern, R, T, widths, value scale), each checked
+40 draws (TS_FUZZ_SEEDS in the environment sets another count) of (entry
+point, pattern, R, T, widths, value scale), each checked
 with the same tolerances as the targeted parity tests: sums and copies
 bit-exact, bf16 norms within 1 ulp (>= 99.9 % identical), codes and scale
 factors within one step on <= 1e-4 of elements (or of the groups, <= 1e-3).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -49,7 +52,7 @@ def _check_fused_outputs(pattern, got, want):
         assert (gs != ws).mean() <= 1e-3 and (np.abs(gs - ws) <= np.abs(ws) * 2.0 ** -7).all()
 
 
-@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("seed", range(int(os.environ.get("TS_FUZZ_SEEDS", "40"))))
 def test_random_configuration(dev, seed):
     rng, kind = _draw(seed)
     scale = float(2.0 ** rng.integers(-8, 9))
