@@ -28,6 +28,7 @@ namespace tsfn {
 namespace {
 
 constexpr int kMaxThreads = 512;
+constexpr int kMaxThreadsPaired = 1024;  // the two-chunk layout as pairs of one-chunk threads
 
 // Register cap per instance (CTAs have at most kMaxThreads = 512 threads, so
 // every cap <= 128 keeps a full CTA launchable): at most 8 partials and 2
@@ -50,10 +51,16 @@ constexpr int load_group()
     return (RB <= 4 && V <= 2) ? V : 1;
 }
 
-template <int RB, int V, Epilogue EP, bool ADD>
+// PAIRED (with V = 1): the two-chunk layout of nthr/2 threads spread over nthr
+// threads, thread i holding the first chunk of a two-chunk thread and thread
+// i + nthr/2 its second.  The first passes its running sum of squares to the
+// second, which continues the same chain, so every value and every rounding
+// is the one of the two-chunk layout: a row's outputs do not depend on T.
+template <int RB, int V, Epilogue EP, bool ADD, bool PAIRED>
 __global__ void __maxnreg__((reg_cap<RB, V>()))
     fused_rows_kernel(const __grid_constant__ FusedArgs a)
 {
+    static_assert(!PAIRED || V == 1, "pairs are of one-chunk threads");
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const int lane = tid & 31;
@@ -141,7 +148,8 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         x[v][e] = acc[e];
-                        ss = fmaf(x[v][e], x[v][e], ss);
+                        if constexpr (!PAIRED)
+                            ss = fmaf(x[v][e], x[v][e], ss);
                     }
                     st_v4(a.residual_out + off, pack8(x[v]));
                 }
@@ -173,15 +181,38 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
         }
     }
 
+    if constexpr (PAIRED) {
+        __shared__ float carry[kMaxThreadsPaired / 2];
+        const int half = nthr >> 1;  // < nc: every first chunk is a real one
+        if (tid < half) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                ss = fmaf(x[0][e], x[0][e], ss);
+            carry[tid] = ss;
+        }
+        __syncthreads();
+        if (tid >= half) {
+            ss = carry[tid - half];
+            if (tid < nc) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    ss = fmaf(x[0][e], x[0][e], ss);
+            }
+        }
+    }
+
     // ---- row reduction of x^2 (the same bits in every thread) --------------
+    // (paired: the upper half's warps hold the sums, in the lower half's order)
     __shared__ float red[kMaxThreads / 32];
     ss = warp_sum(ss);
-    if (lane == 0)
-        red[tid >> 5] = ss;
+    const int nred = PAIRED ? (nthr >> 6) : (nthr >> 5);
+    const int wred = PAIRED ? (tid >> 5) - nred : (tid >> 5);
+    if (lane == 0 && wred >= 0)
+        red[wred] = ss;
     __syncthreads();
     // every warp folds the per-warp sums with the same butterfly, so every
     // thread gets the same bits (each step adds the same two values)
-    const float tot = warp_sum(lane < (nthr >> 5) ? red[lane] : 0.0f);
+    const float tot = warp_sum(lane < nred ? red[lane] : 0.0f);
     const float scale = rsqrtf(__fadd_rn(__fdiv_rn(tot, (float)a.H), a.eps));
 
     float qscale = 0.0f;
@@ -292,26 +323,26 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     }
 }
 
-template <int RB, int V>
+template <int RB, int V, bool PAIRED = false>
 cudaError_t launch_rb_v(Epilogue ep, const FusedArgs &a, int nthr, int64_t grid, bool pdl, cudaStream_t s)
 {
     const dim3 g((unsigned)grid), b((unsigned)nthr);
     const bool add = a.add_in != nullptr;  // only with kNorm / kFp8Block (the reduce-scatter Add codes)
     switch (ep) {
     case Epilogue::kAllReduce:
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kAllReduce, false>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kAllReduce, false, PAIRED>, g, b, 0, s, pdl, a);
     case Epilogue::kNorm:
         if (add)
-            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, true>, g, b, 0, s, pdl, a);
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, false>, g, b, 0, s, pdl, a);
+            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, true, PAIRED>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, false, PAIRED>, g, b, 0, s, pdl, a);
     case Epilogue::kFp8Tensor:
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Tensor, false>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Tensor, false, PAIRED>, g, b, 0, s, pdl, a);
     case Epilogue::kFp4:
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp4, false>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp4, false, PAIRED>, g, b, 0, s, pdl, a);
     case Epilogue::kFp8Block:
         if (add)
-            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, true>, g, b, 0, s, pdl, a);
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, false>, g, b, 0, s, pdl, a);
+            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, true, PAIRED>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, false, PAIRED>, g, b, 0, s, pdl, a);
     }
     return cudaErrorInvalidValue;
 }
@@ -324,12 +355,21 @@ cudaError_t launch_rb(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t s)
     const int per = (nc + V - 1) / V;
     const int nthr = (per + 31) / 32 * 32;
     const int64_t grid = (ep == Epilogue::kFp4 && a.sf_layout != kSfLinear) ? a.sf_rows : a.T;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 0;
     FusedArgs b = a;
     b.prefetch_rows = 0;
+    // Rows that fit one wave of one CTA per SM: each two-chunk thread becomes
+    // a pair of one-chunk threads, so that a thread waits for one set of loads
+    // instead of two (same results, see PAIRED).
+    if constexpr (RB <= 8) {
+        if (V == 2 && sms > 0 && a.T <= sms)
+            return launch_rb_v<RB, 1, true>(ep, b, 2 * nthr, grid, pdl, s);
+    }
     if (RB <= 4) {  // one wave ahead: SMs x CTAs per SM at the instance's register cap
-        int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0) {
+        if (sms > 0) {
             const int cap = V <= 2 ? reg_cap<RB, 2>() : reg_cap<RB, 4>();
             int per_sm = 65536 / (nthr * cap);
             per_sm = per_sm < 2048 / nthr ? per_sm : 2048 / nthr;
