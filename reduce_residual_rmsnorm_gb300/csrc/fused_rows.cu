@@ -51,21 +51,27 @@ constexpr int load_group()
     return (RB <= 4 && V <= 2) ? V : 1;
 }
 
-// PAIRED (with V = 1): the two-chunk layout of nthr/2 threads spread over nthr
-// threads, thread i holding the first chunk of a two-chunk thread and thread
-// i + nthr/2 its second.  The first passes its running sum of squares to the
-// second, which continues the same chain, so every value and every rounding
-// is the one of the two-chunk layout: a row's outputs do not depend on T.
+// PAIRED: the layout of 2V chunks per thread on nthr/2 threads, spread over
+// nthr threads of V chunks.  Thread i holds the first V chunks of a 2V-chunk
+// thread and thread i + nthr/2 the last V; the first passes its running sum
+// of squares to the second, which continues the same chain, so every value
+// and every rounding is the one of the 2V-chunk layout: a row's outputs do
+// not depend on T.
 template <int RB, int V, Epilogue EP, bool ADD, bool PAIRED>
 __global__ void __maxnreg__((reg_cap<RB, V>()))
     fused_rows_kernel(const __grid_constant__ FusedArgs a)
 {
-    static_assert(!PAIRED || V == 1, "pairs are of one-chunk threads");
+    static_assert(!PAIRED || V <= 2, "pairs of one- or two-chunk threads");
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const int lane = tid & 31;
     const int64_t row = blockIdx.x;
     const int nc = (int)(a.H >> 3);
+    // chunk v of this thread: cbase + v * cstride (tid + v * nthr unpaired;
+    // paired, the upper half continues where the lower half's chunks end)
+    const int nhalf = nthr >> 1;
+    const int cstride = PAIRED ? nhalf : nthr;
+    const int cbase = (PAIRED && tid >= nhalf) ? tid + (V - 1) * nhalf : tid;
 
     pdl_wait();
     if constexpr (EP == Epilogue::kFp4) {
@@ -105,13 +111,16 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     float ss = 0.0f;
 
     // ---- phase 1: sum of partials (+ residual), sum of squares ------------
-    constexpr int kGroup = load_group<RB, V>();
+    // (paired with add_in and 3-4 partials, the 2 x 6 grouped loads would
+    // not fit 64 registers beside the pairing: one chunk at a time, still
+    // half the sets of loads of the four-chunk layout)
+    constexpr int kGroup = (PAIRED && ADD && RB >= 4) ? 1 : load_group<RB, V>();
 #pragma unroll
     for (int v0 = 0; v0 < V; v0 += kGroup) {
         uint4 raw[kGroup][RB], res[kGroup], addv[kGroup];
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
-            const int c = tid + (v0 + u) * nthr;
+            const int c = cbase + (v0 + u) * cstride;
             if (c < nc) {
                 const int64_t off = rbase + (int64_t)c * 8;
 #pragma unroll
@@ -128,7 +137,7 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
             const int v = v0 + u;
-            const int c = tid + v * nthr;
+            const int c = cbase + v * cstride;
             if (c < nc) {
                 const int64_t off = rbase + (int64_t)c * 8;
                 float acc[8];
@@ -175,7 +184,7 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     if constexpr (kEarlyGamma) {
 #pragma unroll
         for (int v = 0; v < V; ++v) {
-            const int c = tid + v * nthr;
+            const int c = cbase + v * cstride;
             if (c < nc)
                 gv[v] = ld_keep(a.gamma + (int64_t)c * 8);
         }
@@ -183,21 +192,26 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
 
     if constexpr (PAIRED) {
         __shared__ float carry[kMaxThreadsPaired / 2];
-        const int half = nthr >> 1;  // < nc: every first chunk is a real one
-        if (tid < half) {
+        if (tid < nhalf) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                ss = fmaf(x[0][e], x[0][e], ss);
+            for (int v = 0; v < V; ++v)
+                if (cbase + v * cstride < nc) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        ss = fmaf(x[v][e], x[v][e], ss);
+                }
             carry[tid] = ss;
         }
         __syncthreads();
-        if (tid >= half) {
-            ss = carry[tid - half];
-            if (tid < nc) {
+        if (tid >= nhalf) {
+            ss = carry[tid - nhalf];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    ss = fmaf(x[0][e], x[0][e], ss);
-            }
+            for (int v = 0; v < V; ++v)
+                if (cbase + v * cstride < nc) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        ss = fmaf(x[v][e], x[v][e], ss);
+                }
         }
     }
 
@@ -228,7 +242,7 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     // ---- phase 2: norm and the pattern's outputs ----------------------------
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-        const int c = tid + v * nthr;
+        const int c = cbase + v * cstride;
         const bool live = c < nc;
         const int64_t off = rbase + (int64_t)c * 8;
         float nf[8];
@@ -361,12 +375,21 @@ cudaError_t launch_rb(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t s)
         sms = 0;
     FusedArgs b = a;
     b.prefetch_rows = 0;
-    // Rows that fit one wave of one CTA per SM: each two-chunk thread becomes
-    // a pair of one-chunk threads, so that a thread waits for one set of loads
-    // instead of two (same results, see PAIRED).
+    // Rows that fit one wave of one CTA per SM: each thread of 2 chunks
+    // becomes a pair of one-chunk threads, and with at most 4 partials each
+    // thread of 4 chunks a pair of two-chunk threads that issue both chunks'
+    // loads together, so that a thread waits for fewer sets of loads (same
+    // results, see PAIRED).  Single cold calls: R=8 H=7168 T=16 4.08 us
+    // against 4.40; NVFP4 R=4 H=12288 T=16 5.28 against 7.07 (3.51 against
+    // 4.03 in a CUDA graph).  With 8 partials the four-chunk rows stay
+    // unpaired: 4.63 us against 4.18 at H=16384 T=16 in a CUDA graph.
     if constexpr (RB <= 8) {
-        if (V == 2 && sms > 0 && a.T <= sms)
-            return launch_rb_v<RB, 1, true>(ep, b, 2 * nthr, grid, pdl, s);
+        if (sms > 0 && a.T <= sms) {
+            if (V == 2) return launch_rb_v<RB, 1, true>(ep, b, 2 * nthr, grid, pdl, s);
+            if constexpr (RB <= 4) {
+                if (V == 4) return launch_rb_v<RB, 2, true>(ep, b, 2 * nthr, grid, pdl, s);
+            }
+        }
     }
     if (RB <= 4) {  // one wave ahead: SMs x CTAs per SM at the instance's register cap
         if (sms > 0) {

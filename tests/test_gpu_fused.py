@@ -464,6 +464,27 @@ def test_pdl_dependent_chain_matches_plain(dev):
 # reduce-scatter fusion restated for one GPU (every rank's slice)
 # ---------------------------------------------------------------------------
 
+INVARIANCE = [(1, 8, 7168), (6, 8, 7168), (3, 4, 5120), (1, 8, 16384), (6, 4, 16384), (3, 2, 12288),
+              (7, 3, 9216), (8, 8, 16384)]
+
+
+@pytest.mark.parametrize("pattern,R,H", INVARIANCE, ids=[f"p{p}-R{r}-H{h}" for p, r, h in INVARIANCE])
+def test_rows_do_not_depend_on_T(dev, pattern, R, H):
+    """The first 64 rows in a call of their own (one wave of rows: paired
+    threads) give the same bits as in a call over 600 rows (the ordinary
+    layout of 2 or 4 chunks per thread)."""
+    T, Tsmall = 600, 64
+    inp = _inputs(R, T, H, seed=pattern + R + H)
+    scale = {2: 40.0, 4: 40.0, 3: 300.0, 5: 300.0}.get(pattern)
+    P = 1024 if pattern in (7, 8) else 0
+    full = _run_gpu(dev, pattern, inp, scale, P)
+    small_inp = {"partials": inp["partials"][:, :Tsmall].contiguous(),
+                 "residual": inp["residual"][:Tsmall].contiguous(), "gamma": inp["gamma"]}
+    small = _run_gpu(dev, pattern, small_inp, scale, P)
+    for k, v in small.items():
+        assert np.array_equal(v, full[k][:Tsmall]), k
+
+
 RS_SHAPES = [(4, 37, 1024), (8, 64, 7168), (3, 2, 256), (2, 16, 4096),
              (1, 1300, 1024)]  # R = 1 beyond one wave of CTAs: the L2 prefetch of add_in runs
 
