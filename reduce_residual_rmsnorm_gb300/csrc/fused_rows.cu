@@ -28,11 +28,13 @@ namespace tsfn {
 namespace {
 
 constexpr int kMaxThreads = 512;
-constexpr int kMaxThreadsPaired = 1024;  // the two-chunk layout as pairs of one-chunk threads
+constexpr int kMaxThreadsPaired = 1024;  // a layout of up to 512 threads spread over pairs (PAIRED)
 
-// Register cap per instance (CTAs have at most kMaxThreads = 512 threads, so
-// every cap <= 128 keeps a full CTA launchable): at most 8 partials and 2
-// chunks per thread must leave room for two 512-thread CTAs per SM (64
+// Register cap per instance (unpaired CTAs have at most kMaxThreads = 512
+// threads, so every cap <= 128 keeps a full CTA launchable; paired CTAs of up
+// to 1024 threads exist only for at most 8 partials and 2 chunks per thread,
+// whose cap of 64 fills the 65536 registers exactly): at most 8 partials and
+// 2 chunks per thread must leave room for two 512-thread CTAs per SM (64
 // registers).  The tests check that no instance spills.
 template <int RB, int V>
 constexpr int reg_cap()

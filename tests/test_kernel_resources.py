@@ -50,7 +50,9 @@ def test_no_kernel_spills(resources):
 
 def test_fused_row_kernel_register_tiers(resources):
     """<= 8 partials, <= 2 chunks per thread: two 512-thread CTAs per SM (64
-    registers), also where a thread issues both chunks' loads together."""
+    registers), also where a thread issues both chunks' loads together; the
+    paired instances (CTAs of up to 1024 threads) are among them and need the
+    64 to be launchable at all."""
     # mangled template arguments: fused_rows_kernel<RB, V, Epilogue, ADD>
     checked = 0
     for name, v in resources.items():
