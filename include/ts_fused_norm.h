@@ -35,6 +35,11 @@
  *   - bf16 tensors are row-major and contiguous unless a leading dimension is
  *     given.  Tensor base pointers must be 16-byte aligned (128-bit vector
  *     access); fp32 scalars / scale arrays need 4-byte alignment.
+ *   - Results are deterministic and per row: a row's (token's) outputs depend
+ *     on its own inputs, R, the widths, the pattern and its scalars only, not
+ *     on T, on the other rows, on the flags or on where the buffers live, so
+ *     the same row gives the same bits in every call (a reduce-scatter slice
+ *     equals the matching rows of the all-reduce form).
  *   - Errors: the return value is TS_OK (0) or a negative ts_status_t.  All
  *     argument checks run on the host before anything is launched, so a
  *     rejected call touches no memory.  ts_last_error_detail() returns a
