@@ -123,3 +123,13 @@ def test_recorded_traffic_table_is_well_formed():
             assert os.path.exists(os.path.join(bench.ROOT, "profiles", prof)), prof
         for key, v in cap["bytes_per_launch"].items():
             assert isinstance(v, int) and v > 0, key
+
+
+def test_sweep_shapes_are_valid_calls():
+    """Every (pattern, R, H) of ``--sweep-t`` is a call the library accepts:
+    H a multiple of the pattern's quantisation group, R and H in range."""
+    group = {3: 16, 5: 16, 6: 128, 7: 128}
+    for p, R, H in bench.SWEEP_SHAPES:
+        assert 0 <= p <= 8 and 1 <= R <= 16 and 8 <= H <= 16384
+        assert H % group.get(p, 8) == 0, (p, H)
+    assert list(bench.SWEEP_TOKENS) == sorted(set(bench.SWEEP_TOKENS)) and bench.SWEEP_TOKENS[0] >= 1
