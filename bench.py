@@ -1,28 +1,39 @@
 """Throughput of the fused reduce -> residual -> RMSNorm (+quant) path on GB300.
 
-One step = one ``ts_fused_reduce_norm(kARResidualRMSNorm)`` call over the
-R=8, T=4096, H=7168 bf16 workload (partials N(0, 0.5^2), residual N(0, 1),
-gamma U(0.5, 1.5), seed 0), inputs resident in HBM, launched with the
-pages' ``launch_with_pdl`` option (programmatic dependent launch: each call
-still waits for the previous one to complete before touching memory).
-Prints one JSON line.
+One step = one ``ts_fused_reduce_norm`` call of
+kARResidualRMSNormPartialOutFP8BlockWiseQuant (pattern 7: residual_out, the
+first 1024 columns of the bf16 norm, FP8 E4M3 codes and fp32 1x128 block
+scales) over the largest workload, R=8, T=8192, H=7168 (bf16 partials
+N(0, 0.5^2), residual N(0, 1), 0.1 % of the partial and residual entries x50,
+gamma U(0.5, 1.5), seed 0), inputs resident in HBM, launched with the pages'
+``launch_with_pdl`` option (programmatic dependent launch: each call still
+waits for the previous one to complete before touching memory).  Consecutive
+steps alternate between two copies of the inputs and outputs, so no step
+touches a cache line the step before it touched.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 ``value`` is tokens (rows) per second over all ranks (each rank runs the
-same per-GPU workload: weak scaling, no collective on the data path).  The
-line also carries the roofline of the kernel (algorithmic bytes / CUDA-event
-time against the measured HBM copy bandwidth), an end-to-end figure through
-the C ABI with host buffers (the call given pinned host inputs and outputs,
-which the kernel reads and writes across the host link; the staged-copy form
-beside it), the CPU
-oracle timed on a bounded sample of rows, the SM clocks sampled during the
-timed region, and ``rows``: the other patterns and workloads timed the same
-way (kAllReduce; FP8 per-tensor, FP8 1x128 blockwise, PartialOut on R=8,
-T=8192; NVFP4 on R=4, T=16384, H=5120 in the three SF layouts; tensor-parallel
-degrees 1, 2 and 4 on T=16384, H=5120; the reduce-scatter and all-gather forms;
-the sharded MiniMax QK-norm and single-matrix norm on R=8, T=32768; and the R=2,
-T=16 latency case).
+same per-GPU workload: weak scaling, no collective on the data path).
+``--gpus N`` without torchrun starts N ranks itself through
+torch.distributed.run; under torchrun it must equal WORLD_SIZE.  The line
+also carries the roofline of the kernel (algorithmic bytes / CUDA-event time
+against the measured HBM copy bandwidth), an end-to-end figure through the
+C ABI with host buffers (the call given pinned host inputs and outputs, which
+the kernel reads and writes across the host link; the staged-copy form beside
+it), the host time of one C-ABI call from a C caller, the CPU oracle timed on
+a bounded sample of rows, the SM clocks sampled during the timed region, and
+``rows``: the other patterns and workloads timed the same way (kAllReduce and
+kARResidualRMSNorm on R=8, T=4096; FP8 per-tensor, FP8 1x128 blockwise,
+PartialOut on R=8, T=8192; NVFP4 on R=4, T=16384, H=5120 in the three SF
+layouts; tensor-parallel degrees 1, 2 and 4 on T=16384, H=5120; the
+reduce-scatter and all-gather forms; the sharded MiniMax QK-norm and
+single-matrix norm on R=8, T=32768; and the R=2, T=16 latency case).
+
+Every timed region starts behind a short spin kernel queued on the stream, so
+that the host has enqueued the region's launches before its start event
+runs: the region then measures the GPU executing them back to back, not the
+host's enqueue latency of its first call.
 
 ``--impl reference`` times the CPU oracle instead (host cores, bounded samples
 of the same workload per step); under torchrun only rank 0 runs it.
@@ -45,8 +56,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fused reduce+RMSNorm(+quant) tokens/s and achieved HBM GB/s vs 8 TB/s, 1×GB300"
-WORKLOAD = ("kARResidualRMSNorm R=8 T=4096 H=7168: bf16 partials ~N(0,0.5^2), residual ~N(0,1), "
-            "gamma ~U(0.5,1.5), eps 1e-6, seed 0")
+HEADLINE = {"key": "C3", "pattern": 7, "partial_cols": 1024}
+WORKLOAD = ("kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024: bf16 partials "
+            "~N(0,0.5^2), residual ~N(0,1), 0.1% of partial and residual entries x50, gamma ~U(0.5,1.5), "
+            "eps 1e-6, seed 0")
+NSETS = 2  # copies of each workload's buffers, alternated between consecutive launches
 EPS = 1e-6
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 10 ** 6
@@ -271,7 +285,7 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
 # CPU oracle timing (the reported baseline, never a target)
 # ---------------------------------------------------------------------------
 
-def oracle_rows_per_second(inp_host: dict, seconds: float, pattern: int = 1):
+def oracle_rows_per_second(inp_host: dict, seconds: float, pattern: int = 1, partial_cols: int = 0):
     import numpy as np
 
     import oracle
@@ -284,7 +298,7 @@ def oracle_rows_per_second(inp_host: dict, seconds: float, pattern: int = 1):
     chunk = 8
     while True:
         rows = (np.arange(chunk) + row) % T
-        oracle.fused_reduce_norm(pattern, parts, res, gamma, EPS, rows=rows)
+        oracle.fused_reduce_norm(pattern, parts, res, gamma, EPS, partial_cols=partial_cols, rows=rows)
         done += chunk
         row = (row + chunk) % T
         el = time.perf_counter() - start
@@ -295,7 +309,7 @@ def oracle_rows_per_second(inp_host: dict, seconds: float, pattern: int = 1):
 def _oracle_worker(args):
     """One process of the all-cores baseline: memory-map the bf16 inputs the
     parent wrote, then run the oracle on this worker's rows for ``seconds``."""
-    path, R, T, H, first, stride, seconds = args
+    path, R, T, H, first, stride, seconds, pattern, partial_cols = args
     import numpy as np
 
     import oracle
@@ -308,7 +322,7 @@ def _oracle_worker(args):
     done, row, start = 0, first, time.perf_counter()
     while True:
         rows = (np.arange(8) * stride + row) % T
-        oracle.fused_reduce_norm(1, parts, res, gamma, EPS, rows=rows)
+        oracle.fused_reduce_norm(pattern, parts, res, gamma, EPS, partial_cols=partial_cols, rows=rows)
         done += 8
         row = (row + 8 * stride) % T
         el = time.perf_counter() - start
@@ -316,7 +330,7 @@ def _oracle_worker(args):
             return done, el
 
 
-def oracle_rows_per_second_all_cores(inp_host: dict, seconds: float):
+def oracle_rows_per_second_all_cores(inp_host: dict, seconds: float, pattern: int = 1, partial_cols: int = 0):
     """The same oracle, one spawned process per host core, each on its own rows
     (a reported baseline only); returns (rows/s, cores)."""
     import concurrent.futures as cf
@@ -340,9 +354,30 @@ def oracle_rows_per_second_all_cores(inp_host: dict, seconds: float):
         wl.bits(inp_host["gamma"]).tofile(path + ".gamma")
         # spawned (not forked) workers; a worker that dies raises instead of hanging
         with cf.ProcessPoolExecutor(cores, mp_context=mp.get_context("spawn")) as ex:
-            futs = [ex.submit(_oracle_worker, (path, R, T, H, i, cores, seconds)) for i in range(cores)]
+            futs = [ex.submit(_oracle_worker, (path, R, T, H, i, cores, seconds, pattern, partial_cols))
+                    for i in range(cores)]
             res = [f.result(timeout=seconds + 300) for f in futs]
     return sum(done / el for done, el in res), cores
+
+
+def headline_config(world: int) -> dict:
+    """The ``config`` of the JSON line; both arms print the same one."""
+    from reduce_residual_rmsnorm_gb300 import workloads as wl
+
+    shape = wl.WORKLOADS[HEADLINE["key"]]
+    nbytes = headline_bytes()
+    return {"workload": WORKLOAD, "pattern": HEADLINE["pattern"], "R": shape.R, "T": shape.T, "H": shape.H,
+            "partial_cols": HEADLINE["partial_cols"], "launch_with_pdl": True, "bytes_per_step": nbytes,
+            "l2": (f"inputs larger than L2 ({nbytes / 1e6:.0f} MB per step > 129 MB), and {NSETS} copies of "
+                   "the inputs and outputs alternated between steps; no flush"),
+            "parallelism": f"replicas x{world} (rows are independent; no collective)"}
+
+
+def headline_bytes() -> int:
+    from reduce_residual_rmsnorm_gb300 import workloads as wl
+
+    shape = wl.WORKLOADS[HEADLINE["key"]]
+    return fused_bytes(HEADLINE["pattern"], shape.R, shape.T, shape.H, HEADLINE["partial_cols"])
 
 
 # ---------------------------------------------------------------------------
@@ -358,30 +393,35 @@ def run_reference(args):
     import oracle
     from reduce_residual_rmsnorm_gb300 import workloads as wl
 
-    shape = wl.WORKLOADS["C2"]
+    shape = wl.WORKLOADS[HEADLINE["key"]]
+    pattern, P = HEADLINE["pattern"], HEADLINE["partial_cols"]
     inp = wl.fused_inputs(shape, seed=0)
     parts = [wl.bits(p) for p in inp["partials"]]
     res, gamma = wl.bits(inp["residual"]), wl.bits(inp["gamma"])
+
+    def rows_call(rows):
+        oracle.fused_reduce_norm(pattern, parts, res, gamma, EPS, partial_cols=P, rows=rows)
+
     t0 = time.perf_counter()
-    oracle.fused_reduce_norm(1, parts, res, gamma, EPS, rows=np.arange(4))
+    rows_call(np.arange(4))
     per_row = (time.perf_counter() - t0) / 4
     budget = 120.0  # seconds for warm-up + timed steps together
     rows_per_step = int(max(1, min(shape.T, budget / max(1, args.steps + args.warmup) / per_row)))
     step_rows = lambda i: (np.arange(rows_per_step) + i * rows_per_step) % shape.T  # noqa: E731
     for i in range(args.warmup):
-        oracle.fused_reduce_norm(1, parts, res, gamma, EPS, rows=step_rows(i))
+        rows_call(step_rows(i))
     t0 = time.perf_counter()
     for i in range(args.steps):
-        oracle.fused_reduce_norm(1, parts, res, gamma, EPS, rows=step_rows(args.warmup + i))
+        rows_call(step_rows(args.warmup + i))
     el = time.perf_counter() - t0
     value = rows_per_step * args.steps / el
-    sample = (f"{rows_per_step} of the {shape.T} rows per step (pattern 1, R=8, H=7168), "
-              f"single-threaded C oracle")
+    sample = (f"{rows_per_step} of the {shape.T} rows per step (pattern {pattern}, R={shape.R}, H={shape.H}, "
+              f"P={P}), single-threaded C oracle")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "pattern": 1, "R": 8, "T": 4096, "H": 7168},
+        "data": "synthetic", "config": headline_config(world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -392,17 +432,45 @@ def run_reference(args):
 # our arm
 # ---------------------------------------------------------------------------
 
-def time_launches(fn, iters: int, stream, warmup: int = 3) -> float:
-    """Average ms per call of ``fn`` (launching on ``stream``), CUDA events."""
+# Host time the Python binding takes to enqueue one call (measured 9-16 us on
+# the Grace host); the gate in front of a timed region lasts long enough for
+# the host to enqueue that many calls.
+GATE_US_PER_LAUNCH = 25.0
+GATE_MAX_LAUNCHES = 512
+SLEEP_CYCLES_PER_US = 2100  # torch.cuda._sleep counts SM clock cycles (at most 2070 MHz here)
+
+
+def gate(stream, launches: int) -> float:
+    """Queue a spin kernel on ``stream`` that keeps the GPU busy while the host
+    enqueues the next ``launches`` calls, so that a start event recorded after
+    it is followed by launches already in the queue.  Returns its nominal
+    length in microseconds."""
     import torch
 
-    for _ in range(warmup):
-        fn()
+    us = min(launches, GATE_MAX_LAUNCHES) * GATE_US_PER_LAUNCH + 100.0
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * SLEEP_CYCLES_PER_US))
+    return us
+
+
+def time_launches(calls, iters: int, stream, warmup: int = 3, launches_per_call: int = 1) -> float:
+    """Average ms per call, CUDA events on ``stream`` around ``iters`` calls.
+
+    ``calls``: one callable, or a list of callables (one per copy of the
+    buffers) taken in turn, so that consecutive calls touch different memory.
+    The region starts behind ``gate``."""
+    import torch
+
+    seq = list(calls) if isinstance(calls, (list, tuple)) else [calls]
+    n = len(seq)
+    for i in range(warmup):
+        seq[i % n]()
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gate(stream, iters * launches_per_call)
     s.record(stream)
-    for _ in range(iters):
-        fn()
+    for i in range(iters):
+        seq[(warmup + i) % n]()
     e.record(stream)
     torch.cuda.synchronize()
     return s.elapsed_time(e) / iters
@@ -413,62 +481,60 @@ def roofline_entry(nbytes: int, ms: float, peak: float) -> dict:
     return {"us": ms * 1e3, "bytes": nbytes, "gbs": gbs, "frac": gbs / peak}
 
 
+def _copies(make, nsets: int = NSETS) -> list:
+    """``nsets`` calls of one workload, call i built by ``make(i)`` on its own
+    copy of the inputs and outputs (copy 0 may use the original tensors)."""
+    return [make(i) for i in range(nsets)]
+
+
 def _case_builders():
-    """name -> builder(dev, stream) returning (call, algorithmic bytes per call, label).
-    Builders allocate their inputs (drawn on the GPU) and outputs."""
+    """name -> (label, builder, traffic key).  builder(dev, stream) returns
+    (calls, algorithmic bytes per call, launches per call); ``calls`` holds one
+    call per copy of the buffers (inputs drawn on the GPU)."""
     import torch
 
     import reduce_residual_rmsnorm_gb300 as pkg
     from reduce_residual_rmsnorm_gb300 import workloads as wl
 
-    def c2(pattern, pdl=False):
-        def build(dev, stream):
-            shape = wl.WORKLOADS["C2"]
-            inp = wl.fused_inputs(shape, seed=0, device=dev)
-            T, H = shape.T, shape.H
-            outs = pkg.new_outputs(pattern, T, H, dev)
-            res = None if pattern == 0 else inp["residual"]
-            gam = None if pattern == 0 else inp["gamma"]
-            call = lambda: pkg.ts_fused_reduce_norm(pattern, inp["partials"], res, gam, EPS,  # noqa: E731
-                                                    launch_with_pdl=pdl, stream=stream, **outs)
-            return call, fused_bytes(pattern, 8, T, H)
-        return build
+    def clone_if(t, i):
+        return t if i == 0 else t.clone()
 
-    def c3(pattern, P=0):
+    def fused(key, pattern, P=0, pdl=False, layout=2, R=None, T=None, H=None):
+        """One AllReduceFusionPattern on a named workload (or an R/T/H variant of
+        it); FP8 per-tensor and NVFP4 scales from the workload's own norm."""
         def build(dev, stream):
-            shape = wl.WORKLOADS["C3"]
+            shape = wl.WORKLOADS[key]
+            if R is not None:
+                shape = wl.FusedShape(R=R, T=T, H=H, p_std=shape.p_std, res_std=shape.res_std,
+                                      outlier_frac=shape.outlier_frac)
             inp = wl.fused_inputs(shape, seed=0, device=dev)
-            T, H = shape.T, shape.H
+            Tn, Hn = shape.T, shape.H
             sf = None
-            if pattern == 2:
-                norm = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+            if pattern in (2, 3, 4, 5):
+                norm = torch.empty((Tn, Hn), dtype=torch.bfloat16, device=dev)
                 pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS,
                                          residual_out=torch.empty_like(norm), norm_out=norm, stream=stream)
-                sf = (448.0 / norm.float().abs().max()).reshape(1).to(torch.float32)
+                top = 2688.0 if pattern in (3, 5) else 448.0
+                sf = (top / norm.float().abs().max()).reshape(1).to(torch.float32)
                 del norm
-            outs = pkg.new_outputs(pattern, T, H, dev, partial_cols=P)
-            call = lambda: pkg.ts_fused_reduce_norm(pattern, inp["partials"], inp["residual"], inp["gamma"],  # noqa
-                                                    EPS, sf, stream=stream, **outs)
-            return call, fused_bytes(pattern, 8, T, H, P)
+
+            def make(i):
+                parts = clone_if(inp["partials"], i)
+                res = None if pattern == 0 else clone_if(inp["residual"], i)
+                gam = None if pattern == 0 else inp["gamma"]
+                outs = pkg.new_outputs(pattern, Tn, Hn, dev, partial_cols=P, sf_layout=layout)
+                extra = {"sf_layout": layout} if pattern in (3, 5) else {}
+                return lambda: pkg.ts_fused_reduce_norm(pattern, parts, res, gam, EPS, sf,  # noqa: E731
+                                                        launch_with_pdl=pdl, stream=stream, **extra, **outs)
+            return _copies(make), fused_bytes(pattern, shape.R, Tn, Hn, P, sf_layout=layout), 1
         return build
 
-    def c4(layout):
-        def build(dev, stream):
-            shape = wl.WORKLOADS["C4"]
-            inp = wl.fused_inputs(shape, seed=0, device=dev)
-            T, H = shape.T, shape.H
-            norm = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-            pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS,
-                                     residual_out=torch.empty_like(norm), norm_out=norm, stream=stream)
-            g = (2688.0 / norm.float().abs().max()).reshape(1).to(torch.float32)
-            del norm
-            outs = pkg.new_outputs(3, T, H, dev, sf_layout=layout)
-            call = lambda: pkg.ts_fused_reduce_norm(3, inp["partials"], inp["residual"], inp["gamma"], EPS,  # noqa
-                                                    g, sf_layout=layout, stream=stream, **outs)
-            return call, fused_bytes(3, 4, T, H, sf_layout=int(layout))
-        return build
-
-    def rs_add(rs_pattern, all_ranks=False):
+    def rs_add(rs_pattern, all_ranks=False, concurrent=False):
+        """R per-rank calls one after the other (launch_with_pdl), one call over
+        every rank's slice (rank -1), or, ``concurrent``, the R per-rank calls
+        on R streams forked from and joined back to ``stream`` (the ranks run
+        at the same time, as on R GPUs), captured once in a CUDA graph that
+        each step replays."""
         def build(dev, stream):
             shape = wl.WORKLOADS["C3"]
             inp = wl.fused_inputs(shape, seed=0, device=dev)
@@ -476,18 +542,36 @@ def _case_builders():
             gen = torch.Generator(device=dev)
             gen.manual_seed(1)
             add = torch.randn((T, H), generator=gen, device=dev).to(torch.bfloat16)
-            calls = []
-            for rank in ([-1] if all_ranks else range(R)):
-                start, count = pkg.rs_token_split(T, R, rank)
-                form = 6 if rs_pattern == 7 else 1
-                outs = pkg.new_outputs(form, count, H, dev)
-                calls.append((rank, add[start:start + count], inp["residual"][start:start + count], outs))
+            ranks = [-1] if all_ranks else list(range(R))
 
-            def call():
-                for rank, a_in, res, outs in calls:
-                    pkg.ts_reducescatter_fused_norm(rs_pattern, inp["partials"], rank, a_in, res, inp["gamma"],
-                                                    EPS, launch_with_pdl=True, stream=stream, **outs)
-            return call, rs_add_bytes(R, T, H, rs_pattern == 7) - (R - 1) * H * 2 * (1 if all_ranks else 0)
+            def make(i):
+                parts, a_all, r_all = clone_if(inp["partials"], i), clone_if(add, i), clone_if(inp["residual"], i)
+                calls = []
+                for rank in ranks:
+                    start, count = pkg.rs_token_split(T, R, rank)
+                    form = 6 if rs_pattern == 7 else 1
+                    outs = pkg.new_outputs(form, count, H, dev)
+                    calls.append((rank, a_all[start:start + count], r_all[start:start + count], outs))
+
+                def call():
+                    for rank, a_in, res, outs in calls:
+                        pkg.ts_reducescatter_fused_norm(rs_pattern, parts, rank, a_in, res, inp["gamma"], EPS,
+                                                        launch_with_pdl=True, stream=stream, **outs)
+                if not concurrent:
+                    return call
+                side = [torch.cuda.Stream(device=dev) for _ in calls]
+                graph = torch.cuda.CUDAGraph()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(graph, stream=stream):
+                    for s2, (rank, a_in, res, outs) in zip(side, calls):
+                        s2.wait_stream(stream)
+                        pkg.ts_reducescatter_fused_norm(rs_pattern, parts, rank, a_in, res, inp["gamma"], EPS,
+                                                        stream=s2, **outs)
+                    for s2 in side:
+                        stream.wait_stream(s2)
+                return graph.replay
+            nbytes = rs_add_bytes(R, T, H, rs_pattern == 7) - (R - 1) * H * 2 * (1 if all_ranks else 0)
+            return _copies(make), nbytes, 1 if concurrent else len(ranks)
         return build
 
     def ag(pattern):
@@ -501,100 +585,110 @@ def _case_builders():
             xg = (torch.rand(q, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
             yg = (torch.rand(kv, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
             e = lambda *sh, dt=torch.bfloat16: torch.empty(sh, dtype=dt, device=dev)  # noqa: E731
-            outs = {"allgather_out": e(T, q + kv + rope)}
-            if pattern == 1:
-                outs.update(x_norm_out=e(T, q), y_norm_out=e(T, kv))
-            elif pattern == 2:
-                outs.update(y_norm_out=e(T, kv), quant_out=e(T, q, dt=torch.uint8),
-                            scale_out=e(T, q // 128, dt=torch.float32))
-            call = lambda: pkg.ts_allgather_fused_norm(pattern, slices, q, kv, rope, xg, yg, EPS, EPS,  # noqa
-                                                       stream=stream, **outs)
-            return call, ag_bytes(pattern, T, q, kv, rope)
+
+            def make(i):
+                ins = [clone_if(x, i) for x in slices]
+                outs = {"allgather_out": e(T, q + kv + rope)}
+                if pattern == 1:
+                    outs.update(x_norm_out=e(T, q), y_norm_out=e(T, kv))
+                elif pattern == 2:
+                    outs.update(y_norm_out=e(T, kv), quant_out=e(T, q, dt=torch.uint8),
+                                scale_out=e(T, q // 128, dt=torch.float32))
+                return lambda: pkg.ts_allgather_fused_norm(pattern, ins, q, kv, rope, xg, yg, EPS, EPS,  # noqa
+                                                           stream=stream, **outs)
+            return _copies(make), ag_bytes(pattern, T, q, kv, rope), 1
         return build
 
     def c5(dev, stream):
         qs = wl.WORKLOADS["C5"]
         qi = wl.qk_inputs(qs, seed=0, device=dev)
-        qo = torch.empty((qs.T, qs.R * qs.q_shard), dtype=torch.bfloat16, device=dev)
-        ko = torch.empty((qs.T, qs.R * qs.k_shard), dtype=torch.bfloat16, device=dev)
-        call = lambda: pkg.ts_qk_norm_sharded(qi["shards"], qs.q_shard, qs.k_shard, qi["q_weight"],  # noqa
-                                              qi["k_weight"], EPS, qo, ko, stream=stream)
-        return call, qk_bytes(qs.R, qs.T, qs.q_shard, qs.k_shard)
+
+        def make(i):
+            sh = clone_if(qi["shards"], i)
+            qo = torch.empty((qs.T, qs.R * qs.q_shard), dtype=torch.bfloat16, device=dev)
+            ko = torch.empty((qs.T, qs.R * qs.k_shard), dtype=torch.bfloat16, device=dev)
+            return lambda: pkg.ts_qk_norm_sharded(sh, qs.q_shard, qs.k_shard, qi["q_weight"],  # noqa: E731
+                                                  qi["k_weight"], EPS, qo, ko, stream=stream)
+        return _copies(make), qk_bytes(qs.R, qs.T, qs.q_shard, qs.k_shard), 1
 
     def single(dev, stream):
         gen = torch.Generator(device=dev)
         gen.manual_seed(0)
-        sh = torch.randn((8, 32768, 768), generator=gen, device=dev).to(torch.bfloat16)
+        sh0 = torch.randn((8, 32768, 768), generator=gen, device=dev).to(torch.bfloat16)
         w = (torch.rand(8 * 768, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
-        so = torch.empty((32768, 8 * 768), dtype=torch.bfloat16, device=dev)
-        call = lambda: pkg.ts_rms_norm_sharded(sh, 768, w, EPS, so, stream=stream)  # noqa: E731
-        return call, rms_sharded_bytes(8, 32768, 768)
+
+        def make(i):
+            sh = clone_if(sh0, i)
+            so = torch.empty((32768, 8 * 768), dtype=torch.bfloat16, device=dev)
+            return lambda: pkg.ts_rms_norm_sharded(sh, 768, w, EPS, so, stream=stream)  # noqa: E731
+        return _copies(make), rms_sharded_bytes(8, 32768, 768), 1
 
     def c1(dev, stream):
         shape = wl.WORKLOADS["C1"]
         inp = wl.fused_inputs(shape, seed=0, device=dev)
         outs = pkg.new_outputs(1, 16, 4096, dev)
+
         def call(pdl=False):
             pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS, stream=stream,
                                      launch_with_pdl=pdl, **outs)
-        return call, fused_bytes(1, 2, 16, 4096)
+        return [call], fused_bytes(1, 2, 16, 4096), 1
 
-    def tp(pattern, R):
-        """Smaller tensor-parallel degrees on the R=4 T=16384 H=5120 shape."""
-        def build(dev, stream):
-            T, H = 16384, 5120
-            inp = wl.fused_inputs(wl.FusedShape(R=R, T=T, H=H), seed=0, device=dev)
-            g = None
-            if pattern in (2, 3):
-                norm = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-                pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS,
-                                         residual_out=torch.empty_like(norm), norm_out=norm, stream=stream)
-                g = ((2688.0 if pattern == 3 else 448.0) / norm.float().abs().max()).reshape(1).to(torch.float32)
-                del norm
-            outs = pkg.new_outputs(pattern, T, H, dev)
-            call = lambda: pkg.ts_fused_reduce_norm(pattern, inp["partials"], inp["residual"],  # noqa: E731
-                                                    inp["gamma"], EPS, g, stream=stream, **outs)
-            return call, fused_bytes(pattern, R, T, H)
-        return build
-
+    tp = lambda pattern, R: fused("C4", pattern, R=R, T=16384, H=5120)  # noqa: E731
     return {
-        "c2-p1": ("kARResidualRMSNorm R=8 T=4096 H=7168 launch_with_pdl", c2(1, True)),
-        "c2-p1-nopdl": ("kARResidualRMSNorm R=8 T=4096 H=7168 (plain launch)", c2(1)),
-        "c2-p0": ("kAllReduce R=8 T=4096 H=7168", c2(0)),
-        "c3-p2": ("kARResidualRMSNormFP8Quant R=8 T=8192 H=7168", c3(2)),
-        "c3-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168", c3(6)),
-        "c3-p7": ("kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024", c3(7, 1024)),
-        "c3-p8": ("kARResidualRMSNormPartialOut R=8 T=8192 H=7168 P=1024", c3(8, 1024)),
-        "c4-p3-linear": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF LINEAR", c4(2)),
-        "c4-p3-swizzled": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF SWIZZLED_128x4", c4(0)),
-        "c4-p3-swizzled8": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF SWIZZLED_8x4", c4(1)),
-        "rs-add": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls)", rs_add(8)),
-        "rs-add-all": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, rank -1 (one call)", rs_add(8, True)),
+        "c3-p7": ("kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024 launch_with_pdl",
+                  fused("C3", 7, 1024, pdl=True), "fused_rows_kernel pattern 7 R=8 T=8192 H=7168 P=1024"),
+        "c3-p7-nopdl": ("kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024 (plain launch)",
+                        fused("C3", 7, 1024), None),
+        "c2-p1": ("kARResidualRMSNorm R=8 T=4096 H=7168 launch_with_pdl", fused("C2", 1, pdl=True),
+                  "fused_rows_kernel pattern 1 R=8 T=4096 H=7168"),
+        "c2-p0": ("kAllReduce R=8 T=4096 H=7168", fused("C2", 0), None),
+        "c3-p2": ("kARResidualRMSNormFP8Quant R=8 T=8192 H=7168", fused("C3", 2), None),
+        "c3-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168", fused("C3", 6),
+                  "fused_rows_kernel pattern 6 R=8 T=8192 H=7168"),
+        "c3-p8": ("kARResidualRMSNormPartialOut R=8 T=8192 H=7168 P=1024", fused("C3", 8, 1024), None),
+        "c4-p3-linear": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF LINEAR", fused("C4", 3, layout=2),
+                         None),
+        "c4-p3-swizzled": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF SWIZZLED_128x4",
+                           fused("C4", 3, layout=0), "fused_rows_kernel pattern 3 R=4 T=16384 H=5120 SWIZZLED_128x4"),
+        "c4-p3-swizzled8": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF SWIZZLED_8x4",
+                            fused("C4", 3, layout=1), None),
+        "rs-add": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls)", rs_add(8), None),
+        "rs-add-all": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, rank -1 (one call)", rs_add(8, True),
+                       "fused_rows_kernel reduce-scatter add pattern 8 R=8 T=8192 H=7168 rank -1"),
         "rs-add-fp8b": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls)",
-                        rs_add(7)),
-        "ag-rms": ("kAllGatherfusedRMS R=8 T=65536 1536|512|64", ag(1)),
-        "ag-rms-fp8b": ("kAllGatherfusedRMSFP8BlockWiseQuant R=8 T=65536 1536|512|64", ag(2)),
-        "c5-qk": ("MiniMax QK-RMSNorm R=8 T=32768 Q=1024 K=128", c5),
-        "single-768": ("single-matrix sharded RMSNorm R=8 T=32768 W=768", single),
-        "tp1-p1": ("kARResidualRMSNorm R=1 T=16384 H=5120", tp(1, 1)),
-        "tp2-p1": ("kARResidualRMSNorm R=2 T=16384 H=5120", tp(1, 2)),
-        "tp2-p3": ("kARResidualRMSNormFP4Quant R=2 T=16384 H=5120 SF LINEAR", tp(3, 2)),
-        "tp2-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=2 T=16384 H=5120", tp(6, 2)),
-        "tp4-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=4 T=16384 H=5120", tp(6, 4)),
-        "c1-p1": ("kARResidualRMSNorm R=2 T=16 H=4096 (latency)", c1),
+                        rs_add(7), None),
+        "rs-add-fp8b-streams": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, all 8 rank slices "
+                                "(8 calls on 8 streams, one CUDA graph)", rs_add(7, concurrent=True), None),
+        "rs-add-streams": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, all 8 rank slices (8 calls on 8 streams, "
+                           "one CUDA graph)", rs_add(8, concurrent=True), None),
+        "rs-add-fp8b-all": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, rank -1 (one call)",
+                            rs_add(7, True), None),
+        "ag-rms": ("kAllGatherfusedRMS R=8 T=65536 1536|512|64", ag(1), None),
+        "ag-rms-fp8b": ("kAllGatherfusedRMSFP8BlockWiseQuant R=8 T=65536 1536|512|64", ag(2),
+                        "ag_norm_kernel pattern 2 R=8 T=65536 1536|512|64"),
+        "c5-qk": ("MiniMax QK-RMSNorm R=8 T=32768 Q=1024 K=128", c5, "qk_norm_kernel R=8 T=32768 Q=1024 K=128"),
+        "single-768": ("single-matrix sharded RMSNorm R=8 T=32768 W=768", single,
+                       "qk_norm_kernel single matrix R=8 T=32768 W=768"),
+        "tp1-p1": ("kARResidualRMSNorm R=1 T=16384 H=5120", tp(1, 1), None),
+        "tp2-p1": ("kARResidualRMSNorm R=2 T=16384 H=5120", tp(1, 2), None),
+        "tp2-p3": ("kARResidualRMSNormFP4Quant R=2 T=16384 H=5120 SF LINEAR", tp(3, 2), None),
+        "tp2-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=2 T=16384 H=5120", tp(6, 2), None),
+        "tp4-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=4 T=16384 H=5120", tp(6, 4), None),
+        "c1-p1": ("kARResidualRMSNorm R=2 T=16 H=4096 (latency, inputs warm in L2)", c1, None),
     }
 
 
-def measure_rows(dev, stream, peak: float, iters: int) -> dict:
+def measure_rows(dev, stream, peak: float, iters: int, only=None) -> dict:
     import torch
 
     rows = {}
-    for key, (label, build) in _case_builders().items():
-        if key == "c2-p1":
+    for key, (label, build, tkey) in _case_builders().items():
+        if key == "c3-p7" or (only is not None and key not in only):
             continue  # the headline step, timed in run_ours
         with torch.cuda.stream(stream):
-            call, nbytes = build(dev, stream)
+            calls, nbytes, per_call = build(dev, stream)
             if key == "c1-p1":  # L2-resident latency case: stream launches and a CUDA graph
+                call = calls[0]
                 ms_stream = time_launches(call, max(iters, 200), stream)
                 graph = torch.cuda.CUDAGraph()
                 call()
@@ -613,8 +707,10 @@ def measure_rows(dev, stream, peak: float, iters: int) -> dict:
                 rows[label] = {"us_stream_launch": ms_stream * 1e3, "us_in_cuda_graph": ms_graph * 1e3,
                                "us_in_cuda_graph_pdl": ms_pdl * 1e3, "bytes": nbytes}
             else:
-                rows[label] = roofline_entry(nbytes, time_launches(call, iters, stream), peak)
-        del call
+                ms = time_launches(calls, iters, stream, launches_per_call=per_call)
+                rows[label] = roofline_entry(nbytes, ms, peak)
+                rows[label]["traffic"] = recorded_traffic(tkey) if tkey else None
+        del calls
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
     return rows
@@ -629,13 +725,13 @@ def profile_case(key: str, launches: int) -> None:
     import __graft_entry__
 
     __graft_entry__.build()
-    label, build = _case_builders()[key]
+    label, build, _ = _case_builders()[key]
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        call, nbytes = build(dev, stream)
+        calls, nbytes, _ = build(dev, stream)
         torch.cuda.synchronize()
-        for _ in range(launches):
-            call()
+        for i in range(launches):
+            calls[i % len(calls)]()
     torch.cuda.synchronize()
     print(json.dumps({"case": key, "label": label, "launches": launches, "bytes_per_launch": nbytes}))
 
@@ -704,8 +800,34 @@ def sweep_t(reps: int = 40) -> None:
             torch.cuda.empty_cache()
 
 
+def c_abi_call_cost():
+    """Host microseconds per C-ABI call from a C99 caller (tests/c_call_cost.c),
+    or a dict with the reason it could not be measured."""
+    import tempfile
+
+    from reduce_residual_rmsnorm_gb300 import build as libbuild
+
+    try:
+        lib = libbuild.build()
+        cuda = os.path.dirname(os.path.dirname(libbuild.nvcc()))
+        libdirs = [d for d in (os.path.join(cuda, "lib64"), os.path.join(cuda, "lib")) if os.path.isdir(d)]
+        with tempfile.TemporaryDirectory() as d:
+            exe = os.path.join(d, "c_call_cost")
+            subprocess.check_call(["gcc", "-std=c99", "-O2", "-I", os.path.join(ROOT, "include"), "-isystem",
+                                   os.path.join(cuda, "include"), os.path.join(ROOT, "tests", "c_call_cost.c"),
+                                   "-o", exe, lib, *[f"-L{x}" for x in libdirs], "-lcudart",
+                                   "-Wl,-rpath," + os.path.dirname(lib), *[f"-Wl,-rpath,{x}" for x in libdirs]])
+            r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+        if r.returncode != 0:
+            return {"unavailable": (r.stdout + r.stderr).strip()[-300:]}
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, RuntimeError) as exc:
+        return {"unavailable": str(exc)[-300:]}
+
+
 def run_ours(args):
-    import numpy as np
+    import statistics as st
+
     import torch
 
     world, rank, local = dist_setup()
@@ -721,34 +843,38 @@ def run_ours(args):
     from reduce_residual_rmsnorm_gb300 import workloads as wl
 
     peak, peak_kind = read_peaks()
-    shape = wl.WORKLOADS["C2"]
+    shape = wl.WORKLOADS[HEADLINE["key"]]
+    pattern, P = HEADLINE["pattern"], HEADLINE["partial_cols"]
     R, T, H = shape.R, shape.T, shape.H
     host_inp = wl.fused_inputs(shape, seed=0)
-    parts = host_inp["partials"].to(dev)
-    res = host_inp["residual"].to(dev)
     gamma = host_inp["gamma"].to(dev)
-    res_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    norm_out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    sets = []
+    for i in range(NSETS):  # step i uses copy i % NSETS of the inputs and outputs
+        sets.append((host_inp["partials"].to(dev), host_inp["residual"].to(dev),
+                     pkg.new_outputs(pattern, T, H, dev, partial_cols=P)))
     stream = torch.cuda.Stream(device=dev)
-    nbytes = fused_bytes(1, R, T, H)
+    nbytes = headline_bytes()
 
-    def step():
-        pkg.ts_fused_reduce_norm(1, parts, res, gamma, EPS, residual_out=res_out, norm_out=norm_out,
-                                 launch_with_pdl=True, stream=stream)
+    def step(i):
+        parts, res, outs = sets[i % NSETS]
+        pkg.ts_fused_reduce_norm(pattern, parts, res, gamma, EPS, launch_with_pdl=True, stream=stream, **outs)
 
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
+        for i in range(args.warmup):
+            step(i)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     with sampler:
         barrier(world)
         torch.cuda.synchronize()
+        gate_us = gate(stream, args.steps)
         ev0.record(stream)
+        t0 = time.perf_counter()
         with torch.cuda.stream(stream):
-            for _ in range(args.steps):
-                step()
+            for i in range(args.steps):
+                step(args.warmup + i)
+        host_s = time.perf_counter() - t0
         ev1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -756,6 +882,20 @@ def run_ours(args):
     ms = max_over_ranks(ms_local, world, dev)
     value = world * T / (ms * 1e-3)
     achieved = nbytes / (ms_local * 1e-3) / 1e9
+
+    # diagnostic pass: an event after every launch (which ends the PDL overlap
+    # of consecutive launches, so each step reads a little slower than in the
+    # timed region)
+    n_diag = min(args.steps, 50)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_diag + 1)]
+    gate(stream, n_diag)
+    evs[0].record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(n_diag):
+            step(i)
+            evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per_step = [evs[i].elapsed_time(evs[i + 1]) * 1e3 for i in range(n_diag)]
 
     # end to end through the C ABI with host buffers.  Headline form: the call
     # is given the pinned host inputs and outputs themselves, and the kernel
@@ -765,22 +905,20 @@ def run_ours(args):
     h_parts = host_inp["partials"].pin_memory()
     h_res = host_inp["residual"].pin_memory()
     h_gamma = host_inp["gamma"].pin_memory()
-    h_out_res = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    h_out_norm = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    d_parts = torch.empty_like(parts)
-    d_res = torch.empty_like(res)
+    h_outs = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in sets[0][2].items()}
+    d_parts, d_res, d_outs = sets[0]
 
     def e2e_step():
-        pkg.ts_fused_reduce_norm(1, h_parts, h_res, h_gamma, EPS, residual_out=h_out_res, norm_out=h_out_norm,
-                                 launch_with_pdl=True, stream=stream)
+        pkg.ts_fused_reduce_norm(pattern, h_parts, h_res, h_gamma, EPS, launch_with_pdl=True, stream=stream,
+                                 **h_outs)
 
     def staged_step():
         d_parts.copy_(h_parts, non_blocking=True)
         d_res.copy_(h_res, non_blocking=True)
-        pkg.ts_fused_reduce_norm(1, d_parts, d_res, gamma, EPS, residual_out=res_out, norm_out=norm_out,
-                                 launch_with_pdl=True, stream=stream)
-        h_out_res.copy_(res_out, non_blocking=True)
-        h_out_norm.copy_(norm_out, non_blocking=True)
+        pkg.ts_fused_reduce_norm(pattern, d_parts, d_res, gamma, EPS, launch_with_pdl=True, stream=stream,
+                                 **d_outs)
+        for k, v in h_outs.items():
+            v.copy_(d_outs[k], non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 20))
     with torch.cuda.stream(stream):
@@ -789,38 +927,46 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     staged_ms = max_over_ranks(staged_ms, world, dev)
     h2d = (h_parts.numel() + h_res.numel() + h_gamma.numel()) * 2
-    d2h = (h_out_res.numel() + h_out_norm.numel()) * 2
-    del h_parts, h_res, h_gamma, h_out_res, h_out_norm, d_parts, d_res
+    d2h = sum(v.numel() * v.element_size() for v in h_outs.values())
+    del h_parts, h_res, h_gamma, h_outs, sets, d_parts, d_res, d_outs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
     rows = None
     if not args.no_rows:
         rows = measure_rows(dev, stream, peak, args.row_iters)
+    call_cost = c_abi_call_cost() if rank == 0 and not args.no_rows else None
 
     cpu = cpu_all = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        rps, done, el = oracle_rows_per_second(host_inp, args.cpu_seconds)
+        rps, done, el = oracle_rows_per_second(host_inp, args.cpu_seconds, pattern, P)
         cpu = {"value": rps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{done} rows of the R=8 T=4096 H=7168 kARResidualRMSNorm workload "
+               "sample": f"{done} rows of the R={R} T={T} H={H} pattern {pattern} (P={P}) workload "
                          f"(8-row batches, wrapping), {el:.1f} s of single-threaded C"}
         if args.cpu_all_cores:
-            rps_all, cores = oracle_rows_per_second_all_cores(host_inp, args.cpu_seconds)
+            rps_all, cores = oracle_rows_per_second_all_cores(host_inp, args.cpu_seconds, pattern, P)
             cpu_all = {"value": rps_all, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                        "sample": f"one spawned process per core, each {args.cpu_seconds:.0f} s on its own rows "
                                  f"of the same workload"}
 
     if rank == 0:
+        key = f"fused_rows_kernel pattern {pattern} R={R} T={T} H={H} P={P}"
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "pattern": 1, "R": R, "T": T, "H": H,
-                       "launch_with_pdl": True, "bytes_per_step": nbytes,
-                       "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB per step > 129 MB); no flush",
-                       "parallelism": f"replicas x{world} (rows are independent; no collective)"},
+            "config": headline_config(world),
             "achieved_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy bandwidth",
-                         "traffic": recorded_traffic("fused_rows_kernel pattern 1 R=8 T=4096 H=7168")},
+                         "traffic": recorded_traffic(key)},
+            "timed_region": {
+                "gate_us": gate_us, "host_us_per_call": host_s / args.steps * 1e6,
+                "per_step_us": [round(x, 2) for x in per_step],
+                "per_step_median_us": st.median(per_step),
+                "note": ("the timed launches sit behind a spin kernel of gate_us, so the region times the GPU "
+                         "running them back to back; per_step_us is a separate pass with an event after every "
+                         "launch (no PDL overlap between launches there)")},
             "e2e": {"value": T * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "mode": "pinned host inputs and outputs passed to the call; the kernel reads and writes "
@@ -830,12 +976,35 @@ def run_ours(args):
                                        "outputs back, on one stream"}},
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_all,
+            "c_abi_host_us_per_call": call_cost,
             "gpu_launches": args.steps,
             "clocks": sampler.summary(),
             "kernel_source_hash": kernel_source_hash(),
             "rows": rows,
         }
         print(json.dumps(line), flush=True)
+
+
+def check_world(gpus: int, env=None) -> str:
+    """How to honour ``--gpus``: "run" (this process is one of the ranks, or
+    N = 1) or "spawn" (start N ranks through torch.distributed.run).  Raises
+    SystemExit when a torchrun world disagrees with --gpus."""
+    env = os.environ if env is None else env
+    if gpus < 1:
+        raise SystemExit(f"--gpus must be >= 1 (got {gpus})")
+    world = env.get("WORLD_SIZE")
+    if world is None:
+        return "spawn" if gpus > 1 else "run"
+    if int(world) != gpus:
+        raise SystemExit(f"--gpus {gpus} but WORLD_SIZE={world}: launch with --nproc-per-node {gpus}")
+    return "run"
+
+
+def spawn_command(argv: list, gpus: int, port: int) -> list:
+    """torch.distributed.run command that starts ``gpus`` ranks of this script
+    with the same arguments (one node, rendezvous on 127.0.0.1)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={gpus}",
+            "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *argv]
 
 
 def main(argv=None):
@@ -854,14 +1023,24 @@ def main(argv=None):
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--sweep-t", action="store_true",
                     help="only print the per-call time of single cold fused calls against T")
+    argv = sys.argv[1:] if argv is None else list(argv)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.sweep_t:
         sweep_t()
-    elif args.profile_case:
+        return
+    if args.profile_case:
         profile_case(args.profile_case, args.launches)
-    elif args.impl == "reference":
+        return
+    if check_world(args.gpus) == "spawn":
+        import socket
+
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        raise SystemExit(subprocess.call(spawn_command(argv, args.gpus, port)))
+    if args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -371,10 +371,7 @@ cudaError_t launch_rb(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t s)
     const int per = (nc + V - 1) / V;
     const int nthr = (per + 31) / 32 * 32;
     const int64_t grid = (ep == Epilogue::kFp4 && a.sf_layout != kSfLinear) ? a.sf_rows : a.T;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 0;
+    const int sms = current_device_sms();
     FusedArgs b = a;
     b.prefetch_rows = 0;
     // Rows that fit one wave of one CTA per SM: each thread of 2 chunks

@@ -2,6 +2,7 @@
 // kernel launchers.  Everything here has already been validated.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <utility>
 
@@ -102,6 +103,35 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Devices whose properties the launchers cache (ordinals 0..kMaxCachedDevices-1;
+// a device beyond that is queried on every call).
+constexpr int kMaxCachedDevices = 64;
+
+// Multiprocessor count of the current device, 0 if it cannot be read.  The
+// driver is asked once per device; later calls only read the current device
+// ordinal (stored in *dev when dev is not null).
+inline int current_device_sms(int *dev = nullptr)
+{
+    static std::atomic<int> cache[kMaxCachedDevices];  // 0: not read yet
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess)
+        return 0;
+    if (dev != nullptr)
+        *dev = d;
+    const bool cached = d >= 0 && d < kMaxCachedDevices;
+    if (cached) {
+        const int v = cache[d].load(std::memory_order_relaxed);
+        if (v > 0)
+            return v;
+    }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || sms < 0)
+        return 0;
+    if (cached && sms > 0)
+        cache[d].store(sms, std::memory_order_relaxed);
+    return sms;
 }
 
 cudaError_t launch_fused(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t stream);

@@ -197,11 +197,24 @@ cudaError_t launch_qkc(const QKArgs &a, int tpc, int nthr, bool pdl, cudaStream_
     // one wave of tokens ahead: SMs x resident CTAs per SM x tokens per CTA
     QKArgs c = a;
     c.prefetch_tokens = 0;
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qk_norm_kernel<QC, KC, tpw>, nthr, 0) == cudaSuccess)
+    int dev = 0;
+    const int sms = current_device_sms(&dev);
+    if (sms > 0) {
+        // resident CTAs per SM of this instance at nthr (a multiple of 32, at
+        // most 16 warps), from the occupancy calculator once per device
+        static std::atomic<int> occupancy[kMaxCachedDevices][17];  // per_sm + 1; 0: not computed
+        const int w = nthr >> 5;
+        const bool cached = dev < kMaxCachedDevices && w <= 16;
+        int per_sm = cached ? occupancy[dev][w].load(std::memory_order_relaxed) - 1 : -1;
+        if (per_sm < 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qk_norm_kernel<QC, KC, tpw>, nthr, 0) !=
+                cudaSuccess)
+                per_sm = 0;
+            else if (cached)
+                occupancy[dev][w].store(per_sm + 1, std::memory_order_relaxed);
+        }
         c.prefetch_tokens = (int64_t)sms * per_sm * per_cta;
+    }
     return launch_kernel(qk_norm_kernel<QC, KC, tpw>, g, b, 0, s, pdl, c, tpc);
 }
 

@@ -133,3 +133,51 @@ def test_sweep_shapes_are_valid_calls():
         assert 0 <= p <= 8 and 1 <= R <= 16 and 8 <= H <= 16384
         assert H % group.get(p, 8) == 0, (p, H)
     assert list(bench.SWEEP_TOKENS) == sorted(set(bench.SWEEP_TOKENS)) and bench.SWEEP_TOKENS[0] >= 1
+
+
+def test_gpus_flag_is_honoured():
+    """--gpus N: one process runs as is; N > 1 outside torchrun starts N ranks;
+    under torchrun N must equal WORLD_SIZE, else the bench exits with an error."""
+    assert bench.check_world(1, {}) == "run"
+    assert bench.check_world(4, {}) == "spawn"
+    assert bench.check_world(2, {"WORLD_SIZE": "2"}) == "run"
+    assert bench.check_world(1, {"WORLD_SIZE": "1"}) == "run"
+    for gpus, world in ((2, "4"), (1, "2"), (8, "1")):
+        with pytest.raises(SystemExit):
+            bench.check_world(gpus, {"WORLD_SIZE": world})
+    with pytest.raises(SystemExit):
+        bench.check_world(0, {})
+
+
+def test_spawn_command_starts_n_local_ranks():
+    cmd = bench.spawn_command(["--gpus", "4", "--steps", "7"], 4, 29512)
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=4" in cmd and "--nnodes=1" in cmd
+    assert "--master-addr=127.0.0.1" in cmd and "--master-port=29512" in cmd
+    assert cmd[-4:] == ["--gpus", "4", "--steps", "7"] and cmd[-5].endswith("bench.py")
+
+
+def test_headline_is_the_largest_workload_and_both_arms_share_its_config():
+    """The headline step is pattern 7 on R=8 T=8192 H=7168: the largest
+    per-call byte count among the patterns that workload is measured on (FP8
+    per tensor, FP8 1x128, PartialOut with and without FP8 1x128), and the
+    reference arm prints the same config as ours."""
+    from reduce_residual_rmsnorm_gb300 import workloads as wl
+
+    c3 = wl.WORKLOADS["C3"]
+    assert bench.headline_bytes() == bench.fused_bytes(7, c3.R, c3.T, c3.H, 1024) == 1251751936
+    for p in (2, 6, 8):
+        assert bench.fused_bytes(p, c3.R, c3.T, c3.H, 1024) < bench.headline_bytes()
+    c2 = wl.WORKLOADS["C2"]
+    assert bench.fused_bytes(1, c2.R, c2.T, c2.H) < bench.headline_bytes()
+    cfg = bench.headline_config(1)
+    assert (cfg["pattern"], cfg["R"], cfg["T"], cfg["H"], cfg["partial_cols"]) == (7, 8, 8192, 7168, 1024)
+    assert cfg["bytes_per_step"] == bench.headline_bytes() and cfg == bench.headline_config(1)
+
+
+def test_every_bench_row_names_a_builder():
+    rows = bench._case_builders()
+    assert "c3-p7" in rows and "c2-p1" in rows
+    for key, (label, build, tkey) in rows.items():
+        assert label and callable(build)
+        assert tkey is None or tkey.split()[0] in ("fused_rows_kernel", "qk_norm_kernel", "ag_norm_kernel")

@@ -344,11 +344,49 @@ def test_full_size_allreduce_rmsnorm(dev):
 
 @pytest.mark.slow
 def test_full_size_in_the_benchmark_configuration(dev):
-    """The headline step as bench.py times it: kARResidualRMSNorm R=8, T=4096,
-    H=7168, residual_out and norm_out only, launch_with_pdl, back-to-back
-    launches on a side stream; every row against the oracle.  Then the same
-    call on pinned host inputs and outputs (the end-to-end form): the same
-    bits as on device buffers."""
+    """The headline step as bench.py times it: pattern 7 (PartialOut + FP8
+    1x128) on R=8, T=8192, H=7168 with outliers, P=1024, launch_with_pdl,
+    back-to-back launches on a side stream alternating between two copies of
+    the inputs and outputs.  Sampled rows against the oracle, every row
+    self-consistent, both copies identical.  Then the same call on pinned host
+    inputs and outputs (the end-to-end form): the same bits as on device
+    buffers."""
+    inp = wl.fused_inputs(wl.WORKLOADS["C3"], seed=0)
+    T, H = inp["residual"].shape
+    P = 1024
+    gamma = inp["gamma"].to(dev)
+    sets = [(inp["partials"].to(dev), inp["residual"].to(dev), pkg.new_outputs(7, T, H, dev, partial_cols=P))
+            for _ in range(2)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for i in range(6):
+            parts, res, outs = sets[i % 2]
+            pkg.ts_fused_reduce_norm(7, parts, res, gamma, EPS, launch_with_pdl=True, stream=s, **outs)
+    torch.cuda.synchronize()
+    got = {k: host(v) for k, v in sets[0][2].items()}
+    other = {k: host(v) for k, v in sets[1][2].items()}
+    for k in got:
+        assert np.array_equal(got[k], other[k]), k
+    rows = _sample_rows(T)
+    _compare_rows(7, got, _oracle(7, inp, 0.0, P, rows=rows), rows)
+    base = _run_gpu(dev, 1, inp, allreduce=False)
+    assert np.array_equal(got["partial_norm_out"], base["norm_out"][:, :P])
+    got["norm_ref"] = base["norm_out"]
+    _self_consistency(7, got, None)
+
+    h_outs = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in sets[0][2].items()}
+    pkg.ts_fused_reduce_norm(7, inp["partials"].pin_memory(), inp["residual"].pin_memory(),
+                             inp["gamma"].pin_memory(), EPS, launch_with_pdl=True, **h_outs)
+    torch.cuda.synchronize()
+    for k, v in h_outs.items():
+        assert np.array_equal(host(v), got[k]), k
+
+
+@pytest.mark.slow
+def test_full_size_in_the_former_benchmark_configuration(dev):
+    """kARResidualRMSNorm R=8, T=4096, H=7168, residual_out and norm_out only,
+    launch_with_pdl, back-to-back launches on a side stream; every row
+    against the oracle."""
     inp = wl.fused_inputs(wl.WORKLOADS["C2"], seed=0)
     T, H = inp["residual"].shape
     parts, res, gamma = inp["partials"].to(dev), inp["residual"].to(dev), inp["gamma"].to(dev)
@@ -360,18 +398,9 @@ def test_full_size_in_the_benchmark_configuration(dev):
             pkg.ts_fused_reduce_norm(1, parts, res, gamma, EPS, residual_out=ro, norm_out=no,
                                      launch_with_pdl=True, stream=s)
     torch.cuda.synchronize()
-    got = {"residual_out": host(ro), "norm_out": host(no)}
     want = _oracle(1, inp)
-    assert np.array_equal(got["residual_out"], want["residual_out"])
-    assert_bf16_close(got["norm_out"], want["norm_out"], 1, 0.999, "norm_out")
-
-    h_ro = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    h_no = torch.empty_like(h_ro).pin_memory()
-    pkg.ts_fused_reduce_norm(1, inp["partials"].pin_memory(), inp["residual"].pin_memory(),
-                             inp["gamma"].pin_memory(), EPS, residual_out=h_ro, norm_out=h_no,
-                             launch_with_pdl=True)
-    torch.cuda.synchronize()
-    assert np.array_equal(host(h_ro), got["residual_out"]) and np.array_equal(host(h_no), got["norm_out"])
+    assert np.array_equal(host(ro), want["residual_out"])
+    assert_bf16_close(host(no), want["norm_out"], 1, 0.999, "norm_out")
 
 
 @pytest.mark.slow
@@ -486,7 +515,9 @@ def test_rows_do_not_depend_on_T(dev, pattern, R, H):
 
 
 RS_SHAPES = [(4, 37, 1024), (8, 64, 7168), (3, 2, 256), (2, 16, 4096),
-             (1, 1300, 1024)]  # R = 1 beyond one wave of CTAs: the L2 prefetch of add_in runs
+             (1, 1300, 1024),   # R = 1 beyond one wave of CTAs: the L2 prefetch of add_in runs
+             (3, 300, 9216),    # slices of 100 rows, 4 chunks a row: paired two-chunk threads, add_in
+             (4, 600, 16384)]   # slices of 150 rows (at most one wave): the same with 4 partials
 
 
 @pytest.mark.parametrize("R,T,H", RS_SHAPES, ids=[f"R{r}-T{t}-H{h}" for r, t, h in RS_SHAPES])
@@ -565,11 +596,14 @@ def test_sum_of_squares_overflow(dev):
             assert (got["norm_out"][0] == 0x0000).all() and (got["norm_out"][1] == 0x8000).all()
 
 
-@pytest.mark.parametrize("R,T,H", [(8, 1000, 7168), (2, 8600, 1024)])
+@pytest.mark.parametrize("R,T,H", [(8, 1000, 7168), (2, 8600, 1024), (3, 450, 9216), (4, 600, 16384)])
 def test_reducescatter_all_ranks_in_one_launch(dev, R, T, H):
     """rank = -1: every rank's slice in one launch equals the per-rank calls
     (with R = 2 over 8600 rows the one launch prefetches into L2, the per-rank
-    calls of 4300 rows do not)."""
+    calls of 4300 rows do not; with 3 or 4 partials and 4 chunks a row the
+    per-rank calls of at most one wave of rows run paired two-chunk threads
+    that take add_in one chunk at a time, the one launch the unpaired four-chunk
+    layout)."""
     inp = _inputs(R, T, H, seed=13)
     g = torch.Generator().manual_seed(5)
     add = torch.randn((T, H), generator=g).to(torch.bfloat16).to(dev)

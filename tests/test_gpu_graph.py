@@ -122,3 +122,43 @@ def test_captured_calls_replay_like_direct_calls(dev):
         assert direct.keys() == replayed.keys()
         for k in direct:
             assert np.array_equal(direct[k], replayed[k]), (seed, k)
+
+
+def test_rank_calls_on_concurrent_streams(dev):
+    """The R per-rank reduce-scatter calls on R streams forked from one stream
+    and joined back, captured in a CUDA graph (the ranks run at the same time,
+    as on R GPUs; their calls share inputs and write disjoint slices): the
+    replay gives the bits of one launch over every rank's slice."""
+    R, T, H = 8, 1000, 7168
+    inp = wl.fused_inputs(wl.FusedShape(R=R, T=T, H=H, p_std=0.5), seed=31)
+    g = torch.Generator().manual_seed(32)
+    add = torch.randn((T, H), generator=g).to(torch.bfloat16).to(dev)
+    parts, res, gamma = inp["partials"].to(dev), inp["residual"].to(dev), inp["gamma"].to(dev)
+    for rs, form in ((7, 6), (8, 1)):
+        whole = pkg.new_outputs(form, T, H, dev)
+        pkg.ts_reducescatter_fused_norm(rs, parts, -1, add, res, gamma, 1e-6, **whole)
+        torch.cuda.synchronize()
+        per = []
+        for rank in range(R):
+            start, count = pkg.rs_token_split(T, R, rank)
+            per.append((rank, start, count, pkg.new_outputs(form, count, H, dev)))
+        main = torch.cuda.Stream(device=dev)
+        side = [torch.cuda.Stream(device=dev) for _ in range(R)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=main):
+            for s2, (rank, start, count, outs) in zip(side, per):
+                s2.wait_stream(main)
+                pkg.ts_reducescatter_fused_norm(rs, parts, rank, add[start:start + count],
+                                                res[start:start + count], gamma, 1e-6, stream=s2, **outs)
+            for s2 in side:
+                main.wait_stream(s2)
+        for _ in range(2):
+            for _, _, _, outs in per:
+                for v in outs.values():
+                    v.zero_()
+            torch.cuda.synchronize()
+            graph.replay()
+            torch.cuda.synchronize()
+            for rank, start, count, outs in per:
+                for k, v in outs.items():
+                    assert np.array_equal(host(v), host(whole[k][start:start + count])), (rs, rank, k)

@@ -31,7 +31,14 @@ def _rank_main(rank, world, port, q):
         local_ms = 1.0 + rank * 0.25  # a slower rank 1
         bench.barrier(world)
         worst = bench.max_over_ranks(local_ms, world)
-        q.put((rank, start, count, worst))
+        # --gpus must match the torchrun world
+        ok = bench.check_world(world) == "run"
+        try:
+            bench.check_world(world + 1)
+            ok = False
+        except SystemExit:
+            pass
+        q.put((rank, start, count, worst, ok))
     finally:
         dist.destroy_process_group()
 
@@ -47,9 +54,10 @@ def test_two_gloo_ranks_split_rows_and_take_the_max_time():
         p.join(timeout=120)
     assert all(p.exitcode == 0 for p in procs)
     res = sorted(q.get(timeout=5) for _ in range(2))
-    (r0, s0, c0, w0), (r1, s1, c1, w1) = res
+    (r0, s0, c0, w0, ok0), (r1, s1, c1, w1, ok1) = res
     assert (s0, c0) == (0, 2050) and (s1, c1) == (2050, 2049)
     assert w0 == w1 == 1.25
+    assert ok0 and ok1
 
 
 @pytest.mark.parametrize("T,W", [(0, 3), (1, 4), (4096, 8), (32768, 3), (7, 7), (5, 2)])
