@@ -17,7 +17,8 @@
 // the others measured, even while it still spilled 3 registers: 115.0 us
 // against 122.2 us with the x norms parked in shared memory for a second
 // pass, 123.8 us at 3 CTAs per SM and 133.3 us with two warps per row (it
-// now takes 111.2 us, without spilling).
+// now takes 111.2 us, without spilling).  Calls of at most half a wave of
+// rows use a second form with one warp per row segment (ag_seg_kernel).
 #include "device_util.cuh"
 #include "launch.h"
 
@@ -27,18 +28,10 @@ namespace {
 
 constexpr int kRowsPerCta = 8;
 
-// At least four 256-thread CTAs (32 warps) per SM: at most 64 registers.
-template <int CPL, int PATTERN>
-__global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_norm_kernel(const __grid_constant__ AGArgs a)
+// Where gathered row t lives: rank `rank`'s slice, local row `local`
+// (T < 2^31: 32-bit arithmetic).
+__device__ __forceinline__ const uint16_t *gathered_row(const AGArgs &a, int64_t t)
 {
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int64_t t = (int64_t)blockIdx.x * kRowsPerCta + warp;
-    pdl_wait();
-    if (t >= a.T)
-        return;
-
-    // which rank's slice holds gathered row t (T < 2^31: 32-bit arithmetic)
     const uint32_t tu = (uint32_t)t, R = (uint32_t)a.R;
     const uint32_t base = (uint32_t)a.T / R, extra = (uint32_t)a.T % R;
     uint32_t rank, local;
@@ -50,27 +43,15 @@ __global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_norm_kernel(const __gr
         rank = extra + t2 / base;
         local = t2 - (rank - extra) * base;
     }
-    const int hidden = a.hidden;
-    const uint16_t *row = a.inputs[rank] + (int64_t)local * hidden;
-    const int nch = hidden >> 3, qc = a.q >> 3, kc = a.kv >> 3;
+    return a.inputs[rank] + (int64_t)local * a.hidden;
+}
 
-    uint4 v[CPL];
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-        const int c = lane + 32 * i;
-        if (c < nch)
-            v[i] = ld_stream(row + (int64_t)c * 8);
-    }
-    pdl_launch_dependents();
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-        const int c = lane + 32 * i;
-        if (c < nch)
-            st_v4(a.allgather_out + t * hidden + (int64_t)c * 8, v[i]);
-    }
-    if constexpr (PATTERN == 0)
-        return;
-
+// The two norms (and the FP8 x blocks) of gathered row t, whose x and y
+// chunks lane + 32 i are in v[i] (the rope chunks are not read).
+template <int CPL, int PATTERN>
+__device__ __forceinline__ void ag_row_norms(const AGArgs &a, int64_t t, int lane, const uint4 (&v)[CPL])
+{
+    const int qc = a.q >> 3, kc = a.kv >> 3;
     float sx = 0.0f, sy = 0.0f;
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
@@ -136,6 +117,146 @@ __global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_norm_kernel(const __gr
     }
 }
 
+// At least four 256-thread CTAs (32 warps) per SM: at most 64 registers.
+template <int CPL, int PATTERN>
+__global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_norm_kernel(const __grid_constant__ AGArgs a)
+{
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kRowsPerCta + warp;
+    pdl_wait();
+    if (t >= a.T)
+        return;
+
+    const int hidden = a.hidden;
+    const uint16_t *row = gathered_row(a, t);
+    const int nch = hidden >> 3;
+
+    uint4 v[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const int c = lane + 32 * i;
+        if (c < nch)
+            v[i] = ld_stream(row + (int64_t)c * 8);
+    }
+    pdl_launch_dependents();
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const int c = lane + 32 * i;
+        if (c < nch)
+            st_v4(a.allgather_out + t * hidden + (int64_t)c * 8, v[i]);
+    }
+    if constexpr (PATTERN != 0)
+        ag_row_norms<CPL, PATTERN>(a, t, lane, v);
+}
+
+// ---------------------------------------------------------------------------
+// Segment form, for calls of fewer rows than one wave of the row kernel: one
+// warp per (gathered row, segment), segment 0 the x columns and segment 1 the
+// y and rope columns.  The two norms do not depend on each other, so the two
+// warps of a row never wait for one another, and a short call spreads its work
+// over twice the warps (R=8, 1536 | 512 | 64: T=1024 3.7 us against 4.5 for
+// the bf16 norms, 5.0 against 5.9 with FP8 1x128; T=16 3.1 against 4.3 and
+// 4.4 against 5.7).  With more rows than warp slots the row kernel is faster
+// (T=4096 bf16 8.6 us against 9.2; T=65536 FP8 109.5 against 125.5: the x
+// warps' FP8 epilogue is then covered by half the warps).
+// ---------------------------------------------------------------------------
+
+template <int CPL, int PATTERN>
+__global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_seg_kernel(const __grid_constant__ AGArgs a)
+{
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * (kRowsPerCta / 2) + (warp >> 1);
+    const int seg = warp & 1;
+    pdl_wait();
+    if (t >= a.T)
+        return;
+
+    const int hidden = a.hidden;
+    const uint16_t *row = gathered_row(a, t);
+    const int qc = a.q >> 3, kc = a.kv >> 3, nch = hidden >> 3;
+    const int c0 = seg ? qc : 0;        // the segment's first chunk
+    const int c1 = seg ? nch : qc;      // one past its last chunk
+    const int cn = seg ? qc + kc : qc;  // one past its last normalised chunk
+    // chunk c sits on lane c % 32, as in the row kernel, so that the per-lane
+    // sums and the warp reduction round the same way: a row's bits do not
+    // depend on which form computed it
+    const int cb = c0 & ~31;
+
+    uint4 v[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const int c = cb + lane + 32 * i;
+        if (c >= c0 && c < c1)
+            v[i] = ld_stream(row + (int64_t)c * 8);
+    }
+    pdl_launch_dependents();
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const int c = cb + lane + 32 * i;
+        if (c >= c0 && c < c1)
+            st_v4(a.allgather_out + t * hidden + (int64_t)c * 8, v[i]);
+    }
+    if constexpr (PATTERN == 0)
+        return;
+
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const int c = cb + lane + 32 * i;
+        if (c >= c0 && c < cn)
+            ss += sumsq_bf16x8(v[i], 0.0f);
+    }
+    ss = warp_sum(ss);
+    const float sc = seg ? rsqrtf(__fadd_rn(__fdiv_rn(ss, (float)a.kv), a.y_eps))
+                         : rsqrtf(__fadd_rn(__fdiv_rn(ss, (float)a.q), a.x_eps));
+    const uint16_t *gamma = seg ? a.y_gamma : a.x_gamma;  // indexed by chunk c - c0
+    uint16_t *norm_out = seg ? a.y_norm_out : a.x_norm_out;
+    const int64_t norm_ld = seg ? a.kv : a.q;
+
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        const int c = cb + lane + 32 * i;
+        const bool live = c >= c0 && c < cn;
+        float nf[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            nf[e] = 0.0f;
+        if (live) {
+            float f[8], g[8];
+            unpack8(v[i], f);
+            unpack8(ld_keep(gamma + (int64_t)(c - c0) * 8), g);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                nf[e] = __fmul_rn(__fmul_rn(f[e], sc), g[e]);
+            const uint4 nb = pack8(nf);
+            if (norm_out != nullptr)
+                st_v4(norm_out + t * norm_ld + (int64_t)(c - c0) * 8, nb);
+            if (PATTERN == 2 && seg == 0)
+                unpack8(nb, nf);  // the quantiser reads the bf16-rounded norm
+        }
+        if (PATTERN == 2 && seg == 0 && 32 * i < qc) {
+            // 16 lanes = one 128-column block of x; every lane of the warp
+            // takes part (x may end half-way through the warp)
+            float amax = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                amax = fmaxf(amax, fabsf(nf[e]));
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            if (live) {
+                const float sg = div_const_rn(amax, 448.0f, kRcp448);
+                if ((c & 15) == 0)
+                    st_f32_wb(a.scale_out + t * (a.q >> 7) + (c >> 4), sg);
+                st_v2(a.quant_out + t * a.q + (int64_t)c * 8,
+                      sg != 0.0f ? e4m3_block_codes(nf, sg) : make_uint2(0, 0));
+            }
+        }
+    }
+}
+
 template <int CPL>
 cudaError_t launch_cpl(const AGArgs &a, bool pdl, cudaStream_t s)
 {
@@ -147,11 +268,42 @@ cudaError_t launch_cpl(const AGArgs &a, bool pdl, cudaStream_t s)
     }
 }
 
+template <int CPL>
+cudaError_t launch_seg(const AGArgs &a, bool pdl, cudaStream_t s)
+{
+    constexpr int rows = kRowsPerCta / 2;
+    const dim3 g((unsigned)((a.T + rows - 1) / rows)), b(kRowsPerCta * 32);
+    switch (a.pattern) {
+    case 0: return launch_kernel(ag_seg_kernel<CPL, 0>, g, b, 0, s, pdl, a);
+    case 1: return launch_kernel(ag_seg_kernel<CPL, 1>, g, b, 0, s, pdl, a);
+    default:
+        // an FP8 x segment of more than 6 chunks per lane does not fit the
+        // register budget without spilling: one warp per row there
+        if constexpr (CPL > 6)
+            return launch_cpl<CPL>(a, pdl, s);
+        else
+            return launch_kernel(ag_seg_kernel<CPL, 2>, g, b, 0, s, pdl, a);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_ag(const AGArgs &a, bool pdl, cudaStream_t stream)
 {
     const int per_lane = (a.hidden / 8 + 31) / 32;  // 1..9
+    const int sms = current_device_sms();
+    if (sms > 0 && a.T <= 16 * (int64_t)sms) {
+        // at most half a wave of the row kernel (a warp per row, 32 warps per
+        // SM): two warps per row, one per segment, still fit one wave
+        const int qc = a.q / 8, nch = a.hidden / 8;
+        const int qpl = (qc + 31) / 32, ypl = (nch + 31) / 32 - qc / 32;
+        const int seg_lane = qpl > ypl ? qpl : ypl;  // chunk slots per lane of the wider segment
+        if (seg_lane <= 1) return launch_seg<1>(a, pdl, stream);
+        if (seg_lane <= 2) return launch_seg<2>(a, pdl, stream);
+        if (seg_lane <= 4) return launch_seg<4>(a, pdl, stream);
+        if (seg_lane <= 6) return launch_seg<6>(a, pdl, stream);
+        return launch_seg<9>(a, pdl, stream);
+    }
     if (per_lane <= 1) return launch_cpl<1>(a, pdl, stream);
     if (per_lane <= 2) return launch_cpl<2>(a, pdl, stream);
     if (per_lane <= 4) return launch_cpl<4>(a, pdl, stream);

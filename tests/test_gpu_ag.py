@@ -69,6 +69,11 @@ CASES = [  # R, T, q, kv, rope
     (3, 7, 1408, 512, 64),     # x ends mid-warp (176 chunks); the last CTA part empty
     (5, 13, 1024, 8, 0),       # just past 4 chunks per lane
     (2, 5, 384, 1024, 8),      # x ends mid-warp, y wider than x
+    # more rows than half a wave (16 per SM): the row kernel instead of one
+    # warp per segment
+    (8, 2600, 1536, 512, 64),
+    (3, 2500, 1408, 512, 64),
+    (5, 2500, 384, 1024, 8),
 ]
 
 
@@ -140,3 +145,19 @@ def test_full_size(dev):
     assert_bf16_close(got["x_norm_out"][rows], want["x_norm_out"], 1, 0.999, "x_norm")
     assert_bf16_close(got["y_norm_out"][rows], want["y_norm_out"], 1, 0.999, "y_norm")
     codes_close(got["quant_out"][rows], want["quant_out"], e4m3_order, 1, 1e-4, "x e4m3")
+
+
+@pytest.mark.parametrize("q,kv,rope", [(1536, 512, 64), (1408, 512, 64), (384, 1024, 8), (128, 8, 0)])
+@pytest.mark.parametrize("pattern", [1, 2])
+def test_rows_do_not_depend_on_T(dev, pattern, q, kv, rope):
+    """The first 40 gathered rows in a call of their own (one warp per row
+    segment) give the same bits as in a call over 5000 rows (one warp per
+    row), also where x ends half-way through a warp."""
+    R, T, Ts = 4, 5000, 40
+    full, slices, xg, yg = _inputs(R, T, q, kv, rope, seed=q + kv + pattern)
+    big = _run(dev, pattern, slices, q, kv, rope, xg, yg)
+    small_full = full[:Ts]
+    small_slices = [small_full[s0:s0 + c].clone() for s0, c in (pkg.rs_token_split(Ts, R, r) for r in range(R))]
+    small = _run(dev, pattern, small_slices, q, kv, rope, xg, yg)
+    for k, v in small.items():
+        assert np.array_equal(v, big[k][:Ts]), k

@@ -66,10 +66,10 @@ def test_fused_row_kernel_register_tiers(resources):
 def test_allgather_norm_kernel_fits_four_ctas_per_sm(resources):
     checked = 0
     for name, v in resources.items():
-        if "ag_norm_kernel" in name:
+        if "ag_norm_kernel" in name or "ag_seg_kernel" in name:
             assert v["regs"] <= 64, (name, v)
             checked += 1
-    assert checked >= 12
+    assert checked >= 26
 
 
 def test_sharded_norm_kernels_keep_four_ctas_per_sm(resources):
