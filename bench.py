@@ -181,7 +181,8 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(key: str):
-    """dram read+write bytes per launch from the committed ncu summary, if it was
+    """dram read+write bytes per step of the benchmark row ``key`` (a
+    ``_case_builders`` name) from the committed ncu captures, if they were
     taken on the kernels as they are now (same source hash); else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
@@ -488,7 +489,7 @@ def _copies(make, nsets: int = NSETS) -> list:
 
 
 def _case_builders():
-    """name -> (label, builder, traffic key).  builder(dev, stream) returns
+    """name -> (label, builder).  builder(dev, stream) returns
     (calls, algorithmic bytes per call, launches per call); ``calls`` holds one
     call per copy of the buffers (inputs drawn on the GPU)."""
     import torch
@@ -636,45 +637,39 @@ def _case_builders():
     tp = lambda pattern, R: fused("C4", pattern, R=R, T=16384, H=5120)  # noqa: E731
     return {
         "c3-p7": ("kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024 launch_with_pdl",
-                  fused("C3", 7, 1024, pdl=True), "fused_rows_kernel pattern 7 R=8 T=8192 H=7168 P=1024"),
+                  fused("C3", 7, 1024, pdl=True)),
         "c3-p7-nopdl": ("kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024 (plain launch)",
-                        fused("C3", 7, 1024), None),
-        "c2-p1": ("kARResidualRMSNorm R=8 T=4096 H=7168 launch_with_pdl", fused("C2", 1, pdl=True),
-                  "fused_rows_kernel pattern 1 R=8 T=4096 H=7168"),
-        "c2-p0": ("kAllReduce R=8 T=4096 H=7168", fused("C2", 0), None),
-        "c3-p2": ("kARResidualRMSNormFP8Quant R=8 T=8192 H=7168", fused("C3", 2), None),
-        "c3-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168", fused("C3", 6),
-                  "fused_rows_kernel pattern 6 R=8 T=8192 H=7168"),
-        "c3-p8": ("kARResidualRMSNormPartialOut R=8 T=8192 H=7168 P=1024", fused("C3", 8, 1024), None),
-        "c4-p3-linear": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF LINEAR", fused("C4", 3, layout=2),
-                         None),
+                        fused("C3", 7, 1024)),
+        "c2-p1": ("kARResidualRMSNorm R=8 T=4096 H=7168 launch_with_pdl", fused("C2", 1, pdl=True)),
+        "c2-p0": ("kAllReduce R=8 T=4096 H=7168", fused("C2", 0)),
+        "c3-p2": ("kARResidualRMSNormFP8Quant R=8 T=8192 H=7168", fused("C3", 2)),
+        "c3-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168", fused("C3", 6)),
+        "c3-p8": ("kARResidualRMSNormPartialOut R=8 T=8192 H=7168 P=1024", fused("C3", 8, 1024)),
+        "c4-p3-linear": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF LINEAR", fused("C4", 3, layout=2)),
         "c4-p3-swizzled": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF SWIZZLED_128x4",
-                           fused("C4", 3, layout=0), "fused_rows_kernel pattern 3 R=4 T=16384 H=5120 SWIZZLED_128x4"),
+                           fused("C4", 3, layout=0)),
         "c4-p3-swizzled8": ("kARResidualRMSNormFP4Quant R=4 T=16384 H=5120 SF SWIZZLED_8x4",
-                            fused("C4", 3, layout=1), None),
-        "rs-add": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls)", rs_add(8), None),
-        "rs-add-all": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, rank -1 (one call)", rs_add(8, True),
-                       "fused_rows_kernel reduce-scatter add pattern 8 R=8 T=8192 H=7168 rank -1"),
+                            fused("C4", 3, layout=1)),
+        "rs-add": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls)", rs_add(8)),
+        "rs-add-all": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, rank -1 (one call)", rs_add(8, True)),
         "rs-add-fp8b": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls)",
-                        rs_add(7), None),
+                        rs_add(7)),
         "rs-add-fp8b-streams": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, all 8 rank slices "
-                                "(8 calls on 8 streams, one CUDA graph)", rs_add(7, concurrent=True), None),
+                                "(8 calls on 8 streams, one CUDA graph)", rs_add(7, concurrent=True)),
         "rs-add-streams": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, all 8 rank slices (8 calls on 8 streams, "
-                           "one CUDA graph)", rs_add(8, concurrent=True), None),
+                           "one CUDA graph)", rs_add(8, concurrent=True)),
         "rs-add-fp8b-all": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, rank -1 (one call)",
-                            rs_add(7, True), None),
-        "ag-rms": ("kAllGatherfusedRMS R=8 T=65536 1536|512|64", ag(1), None),
-        "ag-rms-fp8b": ("kAllGatherfusedRMSFP8BlockWiseQuant R=8 T=65536 1536|512|64", ag(2),
-                        "ag_norm_kernel pattern 2 R=8 T=65536 1536|512|64"),
-        "c5-qk": ("MiniMax QK-RMSNorm R=8 T=32768 Q=1024 K=128", c5, "qk_norm_kernel R=8 T=32768 Q=1024 K=128"),
-        "single-768": ("single-matrix sharded RMSNorm R=8 T=32768 W=768", single,
-                       "qk_norm_kernel single matrix R=8 T=32768 W=768"),
-        "tp1-p1": ("kARResidualRMSNorm R=1 T=16384 H=5120", tp(1, 1), None),
-        "tp2-p1": ("kARResidualRMSNorm R=2 T=16384 H=5120", tp(1, 2), None),
-        "tp2-p3": ("kARResidualRMSNormFP4Quant R=2 T=16384 H=5120 SF LINEAR", tp(3, 2), None),
-        "tp2-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=2 T=16384 H=5120", tp(6, 2), None),
-        "tp4-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=4 T=16384 H=5120", tp(6, 4), None),
-        "c1-p1": ("kARResidualRMSNorm R=2 T=16 H=4096 (latency, inputs warm in L2)", c1, None),
+                            rs_add(7, True)),
+        "ag-rms": ("kAllGatherfusedRMS R=8 T=65536 1536|512|64", ag(1)),
+        "ag-rms-fp8b": ("kAllGatherfusedRMSFP8BlockWiseQuant R=8 T=65536 1536|512|64", ag(2)),
+        "c5-qk": ("MiniMax QK-RMSNorm R=8 T=32768 Q=1024 K=128", c5),
+        "single-768": ("single-matrix sharded RMSNorm R=8 T=32768 W=768", single),
+        "tp1-p1": ("kARResidualRMSNorm R=1 T=16384 H=5120", tp(1, 1)),
+        "tp2-p1": ("kARResidualRMSNorm R=2 T=16384 H=5120", tp(1, 2)),
+        "tp2-p3": ("kARResidualRMSNormFP4Quant R=2 T=16384 H=5120 SF LINEAR", tp(3, 2)),
+        "tp2-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=2 T=16384 H=5120", tp(6, 2)),
+        "tp4-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=4 T=16384 H=5120", tp(6, 4)),
+        "c1-p1": ("kARResidualRMSNorm R=2 T=16 H=4096 (latency, inputs warm in L2)", c1),
     }
 
 
@@ -682,7 +677,7 @@ def measure_rows(dev, stream, peak: float, iters: int, only=None) -> dict:
     import torch
 
     rows = {}
-    for key, (label, build, tkey) in _case_builders().items():
+    for key, (label, build) in _case_builders().items():
         if key == "c3-p7" or (only is not None and key not in only):
             continue  # the headline step, timed in run_ours
         with torch.cuda.stream(stream):
@@ -709,7 +704,7 @@ def measure_rows(dev, stream, peak: float, iters: int, only=None) -> dict:
             else:
                 ms = time_launches(calls, iters, stream, launches_per_call=per_call)
                 rows[label] = roofline_entry(nbytes, ms, peak)
-                rows[label]["traffic"] = recorded_traffic(tkey) if tkey else None
+                rows[label]["traffic"] = recorded_traffic(key)
         del calls
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
@@ -725,7 +720,7 @@ def profile_case(key: str, launches: int) -> None:
     import __graft_entry__
 
     __graft_entry__.build()
-    label, build, _ = _case_builders()[key]
+    label, build = _case_builders()[key]
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         calls, nbytes, _ = build(dev, stream)
@@ -950,7 +945,6 @@ def run_ours(args):
                                  f"of the same workload"}
 
     if rank == 0:
-        key = f"fused_rows_kernel pattern {pattern} R={R} T={T} H={H} P={P}"
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -959,7 +953,7 @@ def run_ours(args):
             "achieved_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": f"{peak_kind} HBM copy bandwidth",
-                         "traffic": recorded_traffic(key)},
+                         "traffic": recorded_traffic("c3-p7")},
             "timed_region": {
                 "gate_us": gate_us, "host_us_per_call": host_s / args.steps * 1e6,
                 "per_step_us": [round(x, 2) for x in per_step],

@@ -178,6 +178,14 @@ def test_headline_is_the_largest_workload_and_both_arms_share_its_config():
 def test_every_bench_row_names_a_builder():
     rows = bench._case_builders()
     assert "c3-p7" in rows and "c2-p1" in rows
-    for key, (label, build, tkey) in rows.items():
+    for key, (label, build) in rows.items():
         assert label and callable(build)
-        assert tkey is None or tkey.split()[0] in ("fused_rows_kernel", "qk_norm_kernel", "ag_norm_kernel")
+
+
+def test_recorded_traffic_names_bench_rows():
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    rows = bench._case_builders()
+    for cap in rec["captures"].values():
+        for key in cap["bytes_per_launch"]:
+            assert key in rows, key
