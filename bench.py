@@ -141,6 +141,12 @@ def read_peaks() -> tuple[float, str]:
 
 
 KERNEL_SOURCES = ("ag_norm.cu", "device_util.cuh", "fused_rows.cu", "launch.h", "qk_norm.cu", "sf_layout.cuh")
+# the device sources each kernel family is built from
+KERNEL_FAMILIES = {
+    "fused_rows": ("device_util.cuh", "fused_rows.cu", "launch.h", "sf_layout.cuh"),
+    "qk_norm": ("device_util.cuh", "launch.h", "qk_norm.cu"),
+    "ag_norm": ("ag_norm.cu", "device_util.cuh", "launch.h"),
+}
 
 
 def _code_tokens(text: str) -> str:
@@ -168,29 +174,43 @@ def _code_tokens(text: str) -> str:
     return " ".join("".join(out).split())
 
 
-def kernel_source_hash() -> str:
-    """Hash of the device code (not the host-side argument checks), comments
-    and layout excluded."""
-    h = hashlib.sha256()
+def kernel_source_hash(files=KERNEL_SOURCES, read=None) -> str:
+    """Hash of device sources (by default all of them; not the host-side
+    argument checks), comments and layout excluded.  ``read(name)`` returns a
+    file's text (default: the file under csrc/)."""
     csrc = os.path.join(ROOT, "reduce_residual_rmsnorm_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn in KERNEL_SOURCES:
+    if read is None:
+        def read(fn):
             with open(os.path.join(csrc, fn), encoding="utf-8") as f:
-                h.update(fn.encode() + b"\0" + _code_tokens(f.read()).encode())
+                return f.read()
+    h = hashlib.sha256()
+    for fn in sorted(files):
+        h.update(fn.encode() + b"\0" + _code_tokens(read(fn)).encode())
     return h.hexdigest()[:16]
 
 
+def row_family(key: str) -> str:
+    """Kernel family a benchmark row (a ``_case_builders`` name) runs."""
+    if key.startswith("ag-"):
+        return "ag_norm"
+    if key in ("c5-qk", "single-768"):
+        return "qk_norm"
+    return "fused_rows"
+
+
 def recorded_traffic(key: str):
-    """dram read+write bytes per step of the benchmark row ``key`` (a
-    ``_case_builders`` name) from the committed ncu captures, if they were
-    taken on the kernels as they are now (same source hash); else None."""
+    """dram read+write bytes per step of the benchmark row ``key`` from the
+    committed ncu captures, if they were taken on that row's kernel as it is
+    now (same hash of its family's sources); else None."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    v = rec.get("captures", {}).get(kernel_source_hash(), {}).get("bytes_per_launch", {}).get(key)
-    return None if v is None else int(v)
+    row = rec.get("rows", {}).get(key)
+    if row is None or row.get("kernel_hash") != kernel_source_hash(KERNEL_FAMILIES[row_family(key)]):
+        return None
+    return int(row["bytes"])
 
 
 class ClockSampler:

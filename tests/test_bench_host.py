@@ -115,14 +115,25 @@ def test_code_tokens_keep_literals():
 
 
 def test_recorded_traffic_table_is_well_formed():
+    """Every record names a benchmark row, a positive byte count, the 16-digit
+    hash of its kernel family's sources and a committed profile summary."""
     with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
         rec = json.load(f)
-    for h, cap in rec["captures"].items():
-        assert len(h) == 16 and int(h, 16) >= 0
-        for prof in cap["profile"].split(", "):
-            assert os.path.exists(os.path.join(bench.ROOT, "profiles", prof)), prof
-        for key, v in cap["bytes_per_launch"].items():
-            assert isinstance(v, int) and v > 0, key
+    rows = bench._case_builders()
+    for key, row in rec["rows"].items():
+        assert key in rows, key
+        assert isinstance(row["bytes"], int) and row["bytes"] > 0, key
+        assert len(row["kernel_hash"]) == 16 and int(row["kernel_hash"], 16) >= 0
+        assert os.path.exists(os.path.join(bench.ROOT, "profiles", row["profile"])), row["profile"]
+
+
+def test_kernel_families_cover_the_sources():
+    fams = set()
+    for files in bench.KERNEL_FAMILIES.values():
+        fams.update(files)
+    assert fams == set(bench.KERNEL_SOURCES)
+    assert bench.row_family("ag-rms-fp8b") == "ag_norm" and bench.row_family("c5-qk") == "qk_norm"
+    assert bench.row_family("c3-p7") == "fused_rows" and bench.row_family("rs-add") == "fused_rows"
 
 
 def test_sweep_shapes_are_valid_calls():
@@ -180,12 +191,3 @@ def test_every_bench_row_names_a_builder():
     assert "c3-p7" in rows and "c2-p1" in rows
     for key, (label, build) in rows.items():
         assert label and callable(build)
-
-
-def test_recorded_traffic_names_bench_rows():
-    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
-        rec = json.load(f)
-    rows = bench._case_builders()
-    for cap in rec["captures"].values():
-        for key in cap["bytes_per_launch"]:
-            assert key in rows, key
