@@ -28,7 +28,9 @@ kARResidualRMSNorm on R=8, T=4096; FP8 per-tensor, FP8 1x128 blockwise,
 PartialOut on R=8, T=8192; NVFP4 on R=4, T=16384, H=5120 in the three SF
 layouts; tensor-parallel degrees 1, 2 and 4 on T=16384, H=5120; the
 reduce-scatter and all-gather forms; the sharded MiniMax QK-norm and
-single-matrix norm on R=8, T=32768; and the R=2, T=16 latency case).
+single-matrix norm on R=8, T=32768; and the R=2, T=16 latency case).  Rows
+launch with ``launch_with_pdl`` too, except those labelled "(plain launch)"
+and the reduce-scatter calls on concurrent streams.
 
 Every timed region starts behind a short spin kernel queued on the stream, so
 that the host has enqueued the region's launches before its start event
@@ -520,7 +522,7 @@ def _case_builders():
     def clone_if(t, i):
         return t if i == 0 else t.clone()
 
-    def fused(key, pattern, P=0, pdl=False, layout=2, R=None, T=None, H=None):
+    def fused(key, pattern, P=0, pdl=True, layout=2, R=None, T=None, H=None):
         """One AllReduceFusionPattern on a named workload (or an R/T/H variant of
         it); FP8 per-tensor and NVFP4 scales from the workload's own norm."""
         def build(dev, stream):
@@ -616,7 +618,7 @@ def _case_builders():
                     outs.update(y_norm_out=e(T, kv), quant_out=e(T, q, dt=torch.uint8),
                                 scale_out=e(T, q // 128, dt=torch.float32))
                 return lambda: pkg.ts_allgather_fused_norm(pattern, ins, q, kv, rope, xg, yg, EPS, EPS,  # noqa
-                                                           stream=stream, **outs)
+                                                           launch_with_pdl=True, stream=stream, **outs)
             return _copies(make), ag_bytes(pattern, T, q, kv, rope), 1
         return build
 
@@ -629,7 +631,8 @@ def _case_builders():
             qo = torch.empty((qs.T, qs.R * qs.q_shard), dtype=torch.bfloat16, device=dev)
             ko = torch.empty((qs.T, qs.R * qs.k_shard), dtype=torch.bfloat16, device=dev)
             return lambda: pkg.ts_qk_norm_sharded(sh, qs.q_shard, qs.k_shard, qi["q_weight"],  # noqa: E731
-                                                  qi["k_weight"], EPS, qo, ko, stream=stream)
+                                                  qi["k_weight"], EPS, qo, ko, launch_with_pdl=True,
+                                                  stream=stream)
         return _copies(make), qk_bytes(qs.R, qs.T, qs.q_shard, qs.k_shard), 1
 
     def single(dev, stream):
@@ -641,7 +644,8 @@ def _case_builders():
         def make(i):
             sh = clone_if(sh0, i)
             so = torch.empty((32768, 8 * 768), dtype=torch.bfloat16, device=dev)
-            return lambda: pkg.ts_rms_norm_sharded(sh, 768, w, EPS, so, stream=stream)  # noqa: E731
+            return lambda: pkg.ts_rms_norm_sharded(sh, 768, w, EPS, so, launch_with_pdl=True,  # noqa: E731
+                                                   stream=stream)
         return _copies(make), rms_sharded_bytes(8, 32768, 768), 1
 
     def c1(dev, stream):
@@ -656,11 +660,11 @@ def _case_builders():
 
     tp = lambda pattern, R: fused("C4", pattern, R=R, T=16384, H=5120)  # noqa: E731
     return {
-        "c3-p7": ("kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024 launch_with_pdl",
-                  fused("C3", 7, 1024, pdl=True)),
+        "c3-p7": ("kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024",
+                  fused("C3", 7, 1024)),
         "c3-p7-nopdl": ("kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024 (plain launch)",
-                        fused("C3", 7, 1024)),
-        "c2-p1": ("kARResidualRMSNorm R=8 T=4096 H=7168 launch_with_pdl", fused("C2", 1, pdl=True)),
+                        fused("C3", 7, 1024, pdl=False)),
+        "c2-p1": ("kARResidualRMSNorm R=8 T=4096 H=7168", fused("C2", 1)),
         "c2-p0": ("kAllReduce R=8 T=4096 H=7168", fused("C2", 0)),
         "c3-p2": ("kARResidualRMSNormFP8Quant R=8 T=8192 H=7168", fused("C3", 2)),
         "c3-p6": ("kARResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168", fused("C3", 6)),
