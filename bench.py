@@ -522,7 +522,7 @@ def _case_builders():
     def clone_if(t, i):
         return t if i == 0 else t.clone()
 
-    def fused(key, pattern, P=0, pdl=True, layout=2, R=None, T=None, H=None):
+    def fused(key, pattern, P=0, pdl=True, layout=2, R=None, T=None, H=None, early=False):
         """One AllReduceFusionPattern on a named workload (or an R/T/H variant of
         it); FP8 per-tensor and NVFP4 scales from the workload's own norm."""
         def build(dev, stream):
@@ -548,11 +548,12 @@ def _case_builders():
                 outs = pkg.new_outputs(pattern, Tn, Hn, dev, partial_cols=P, sf_layout=layout)
                 extra = {"sf_layout": layout} if pattern in (3, 5) else {}
                 return lambda: pkg.ts_fused_reduce_norm(pattern, parts, res, gam, EPS, sf,  # noqa: E731
-                                                        launch_with_pdl=pdl, stream=stream, **extra, **outs)
+                                                        launch_with_pdl=pdl, pdl_early_read=early,
+                                                        stream=stream, **extra, **outs)
             return _copies(make), fused_bytes(pattern, shape.R, Tn, Hn, P, sf_layout=layout), 1
         return build
 
-    def rs_add(rs_pattern, all_ranks=False, concurrent=False):
+    def rs_add(rs_pattern, all_ranks=False, concurrent=False, early=False):
         """R per-rank calls one after the other (launch_with_pdl), one call over
         every rank's slice (rank -1), or, ``concurrent``, the R per-rank calls
         on R streams forked from and joined back to ``stream`` (the ranks run
@@ -579,7 +580,8 @@ def _case_builders():
                 def call():
                     for rank, a_in, res, outs in calls:
                         pkg.ts_reducescatter_fused_norm(rs_pattern, parts, rank, a_in, res, inp["gamma"], EPS,
-                                                        launch_with_pdl=True, stream=stream, **outs)
+                                                        launch_with_pdl=True, pdl_early_read=early,
+                                                        stream=stream, **outs)
                 if not concurrent:
                     return call
                 side = [torch.cuda.Stream(device=dev) for _ in calls]
@@ -664,6 +666,8 @@ def _case_builders():
                   fused("C3", 7, 1024)),
         "c3-p7-nopdl": ("kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024 (plain launch)",
                         fused("C3", 7, 1024, pdl=False)),
+        "c3-p7-early": ("kARResidualRMSNormPartialOutFP8BlockWiseQuant R=8 T=8192 H=7168 P=1024 (inputs read "
+                        "before the wait)", fused("C3", 7, 1024, early=True)),
         "c2-p1": ("kARResidualRMSNorm R=8 T=4096 H=7168", fused("C2", 1)),
         "c2-p0": ("kAllReduce R=8 T=4096 H=7168", fused("C2", 0)),
         "c3-p2": ("kARResidualRMSNormFP8Quant R=8 T=8192 H=7168", fused("C3", 2)),
@@ -678,6 +682,10 @@ def _case_builders():
         "rs-add-all": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, rank -1 (one call)", rs_add(8, True)),
         "rs-add-fp8b": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls)",
                         rs_add(7)),
+        "rs-add-early": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls, inputs read "
+                         "before the wait)", rs_add(8, early=True)),
+        "rs-add-fp8b-early": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, all 8 rank slices (8 PDL "
+                              "calls, inputs read before the wait)", rs_add(7, early=True)),
         "rs-add-fp8b-streams": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, all 8 rank slices "
                                 "(8 calls on 8 streams, one CUDA graph)", rs_add(7, concurrent=True)),
         "rs-add-streams": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, all 8 rank slices (8 calls on 8 streams, "

@@ -82,7 +82,20 @@ enum {
      * (griddepcontrol.wait) for that kernel to complete before it touches any
      * memory, and lets the next kernel start launching once its own loads are
      * issued.  Results are identical with and without the flag. */
-    TS_FLAG_PDL = 1u
+    TS_FLAG_PDL = 1u,
+    /* With TS_FLAG_PDL, for ts_fused_reduce_norm and ts_reducescatter_fused_norm
+     * only: the kernel reads the first part of its inputs (partials, residual,
+     * add_in) before it waits for the previous kernel in the stream, so that
+     * those reads overlap that kernel's last CTAs.  Set it only when the
+     * previous kernel writes none of this call's inputs (for example the
+     * per-rank calls of one reduce-scatter, or calls on buffers produced
+     * earlier); the kernel still waits before it writes any output, so a
+     * previous kernel that reads this call's outputs is safe either way.
+     * Results are identical with and without the flag.  It takes effect where
+     * it measured faster (5 to 8 partials, rows of up to 8192 columns, more
+     * rows than SMs); elsewhere, and without TS_FLAG_PDL, it is accepted and
+     * changes nothing.  An extension: the pages have only launch_with_pdl. */
+    TS_FLAG_PDL_EARLY_READ = 2u
 };
 
 /* Codes identical to `AllReduceFusionPattern` (tokenspeed trtllm.py). */
@@ -191,7 +204,8 @@ typedef struct {
  *   H             hidden size: multiple of 8, <= 16384; multiple of 128 for
  *                 patterns 6, 7; multiple of 16 for patterns 3, 5.
  *   outs          host pointer to the output set (see ts_outs_t).
- *   flags         0 or TS_FLAG_PDL; other bits: TS_ERR_UNSUPPORTED.
+ *   flags         0, TS_FLAG_PDL, or TS_FLAG_PDL | TS_FLAG_PDL_EARLY_READ; other
+ *                 bits: TS_ERR_UNSUPPORTED.
  *   stream        cudaStream_t.
  */
 TS_API int ts_fused_reduce_norm(int pattern, const void *const *partials, int R, const void *residual,

@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_norm_kernel(const __gr
 }
 
 // ---------------------------------------------------------------------------
-// Segment form, for calls of fewer rows than one wave of the row kernel: one
-// warp per (gathered row, segment), segment 0 the x columns and segment 1 the
+// Segment form, for calls of at most half a wave of the row kernel (16 rows
+// per SM): one warp per (gathered row, segment), segment 0 the x columns and segment 1 the
 // y and rope columns.  The two norms do not depend on each other, so the two
 // warps of a row never wait for one another, and a short call spreads its work
 // over twice the warps (R=8, 1536 | 512 | 64: T=1024 3.7 us against 4.5 for

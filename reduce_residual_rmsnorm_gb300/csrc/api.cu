@@ -83,7 +83,8 @@ const char *const kOutputNames[6] = {"allreduce_out", "residual_out", "norm_out"
                                      "partial_norm_out", "quant_out", "scale_out"};
 
 constexpr int64_t kMaxH = 16384;
-constexpr uint32_t kKnownFlags = TS_FLAG_PDL;
+constexpr uint32_t kKnownFlags = TS_FLAG_PDL;                           // sharded and all-gather norms
+constexpr uint32_t kFusedFlags = TS_FLAG_PDL | TS_FLAG_PDL_EARLY_READ;  // fused and reduce-scatter forms
 constexpr int64_t kMaxRows = 0x7FFFFFFFLL;
 
 }  // namespace
@@ -133,8 +134,8 @@ int fused_impl(int pattern, const void *const *partials, int R, const void *add_
         return fail(TS_ERR_SHAPE, "NVFP4 needs H %% 16 == 0 (H = %lld)", (long long)H);
     if (outs->reserved != 0)
         return fail(TS_ERR_UNSUPPORTED, "ts_outs_t.reserved must be 0");
-    if (flags & ~kKnownFlags)
-        return fail(TS_ERR_UNSUPPORTED, "unknown flag bits 0x%x", flags & ~kKnownFlags);
+    if (flags & ~kFusedFlags)
+        return fail(TS_ERR_UNSUPPORTED, "unknown flag bits 0x%x", flags & ~kFusedFlags);
 
     // inputs (with T == 0 the per-row buffers may be NULL: empty tensors)
     const bool empty = T == 0;
@@ -264,6 +265,8 @@ int fused_impl(int pattern, const void *const *partials, int R, const void *add_
     a.sf_layout = layout;
     a.sf_rows = sf_rows;
     a.sf_cols = sf_cols;
+    const bool pdl = (flags & TS_FLAG_PDL) != 0;
+    a.early_read = pdl && (flags & TS_FLAG_PDL_EARLY_READ) ? 1 : 0;
 
     Epilogue ep;
     switch (pattern) {
@@ -276,8 +279,7 @@ int fused_impl(int pattern, const void *const *partials, int R, const void *add_
     case 5: ep = Epilogue::kFp4; break;
     default: ep = Epilogue::kFp8Block; break;
     }
-    const cudaError_t err =
-        tsfn::launch_fused(ep, a, (flags & TS_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream));
+    const cudaError_t err = tsfn::launch_fused(ep, a, pdl, static_cast<cudaStream_t>(stream));
     if (err != cudaSuccess)
         return fail(TS_ERR_LAUNCH, "kernel launch failed: %s (%s)", cudaGetErrorName(err),
                     cudaGetErrorString(err));

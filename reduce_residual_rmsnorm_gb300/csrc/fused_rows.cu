@@ -59,7 +59,12 @@ constexpr int load_group()
 // of squares to the second, which continues the same chain, so every value
 // and every rounding is the one of the 2V-chunk layout: a row's outputs do
 // not depend on T.
-template <int RB, int V, Epilogue EP, bool ADD, bool PAIRED>
+//
+// EARLY (TS_FLAG_PDL_EARLY_READ, the caller's guarantee that the previous
+// kernel in the stream writes none of this call's inputs): the first chunk
+// group's loads are issued before the dependency wait, so they overlap that
+// kernel's last CTAs; nothing is written before the wait.
+template <int RB, int V, Epilogue EP, bool ADD, bool PAIRED, bool EARLY = false>
 __global__ void __maxnreg__((reg_cap<RB, V>()))
     fused_rows_kernel(const __grid_constant__ FusedArgs a)
 {
@@ -74,6 +79,33 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     const int nhalf = nthr >> 1;
     const int cstride = PAIRED ? nhalf : nthr;
     const int cbase = (PAIRED && tid >= nhalf) ? tid + (V - 1) * nhalf : tid;
+
+    // (paired with add_in and 3-4 partials, the 2 x 6 grouped loads would
+    // not fit 64 registers beside the pairing: one chunk at a time, still
+    // half the sets of loads of the four-chunk layout)
+    constexpr int kGroup = (PAIRED && ADD && RB >= 4) ? 1 : load_group<RB, V>();
+    constexpr int kE = EARLY ? kGroup : 1;  // early loads held across the wait
+    uint4 eraw[kE][EARLY ? RB : 1], eres[kE], eadd[kE];
+    if constexpr (EARLY) {
+        if (row < a.T) {
+#pragma unroll
+            for (int u = 0; u < kGroup; ++u) {
+                const int c = cbase + u * cstride;
+                if (c < nc) {
+                    const int64_t off = row * a.H + (int64_t)c * 8;
+#pragma unroll
+                    for (int r = 0; r < RB; ++r)
+                        if (r < a.R)
+                            eraw[u][r] = ld_stream(a.partials[r] + off);
+                    if constexpr (EP != Epilogue::kAllReduce) {
+                        eres[u] = ld_stream(a.residual + off);
+                        if constexpr (ADD)
+                            eadd[u] = ld_stream(a.add_in + off);
+                    }
+                }
+            }
+        }
+    }
 
     pdl_wait();
     if constexpr (EP == Epilogue::kFp4) {
@@ -113,17 +145,19 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     float ss = 0.0f;
 
     // ---- phase 1: sum of partials (+ residual), sum of squares ------------
-    // (paired with add_in and 3-4 partials, the 2 x 6 grouped loads would
-    // not fit 64 registers beside the pairing: one chunk at a time, still
-    // half the sets of loads of the four-chunk layout)
-    constexpr int kGroup = (PAIRED && ADD && RB >= 4) ? 1 : load_group<RB, V>();
 #pragma unroll
     for (int v0 = 0; v0 < V; v0 += kGroup) {
         uint4 raw[kGroup][RB], res[kGroup], addv[kGroup];
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
             const int c = cbase + (v0 + u) * cstride;
-            if (c < nc) {
+            if (EARLY && v0 == 0) {  // loaded before the wait
+#pragma unroll
+                for (int r = 0; r < RB; ++r)
+                    raw[u][r] = eraw[EARLY ? u : 0][EARLY ? r : 0];
+                res[u] = eres[EARLY ? u : 0];
+                addv[u] = eadd[EARLY ? u : 0];
+            } else if (c < nc) {
                 const int64_t off = rbase + (int64_t)c * 8;
 #pragma unroll
                 for (int r = 0; r < RB; ++r)
@@ -339,26 +373,27 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     }
 }
 
-template <int RB, int V, bool PAIRED = false>
+template <int RB, int V, bool PAIRED = false, bool EARLY = false>
 cudaError_t launch_rb_v(Epilogue ep, const FusedArgs &a, int nthr, int64_t grid, bool pdl, cudaStream_t s)
 {
     const dim3 g((unsigned)grid), b((unsigned)nthr);
     const bool add = a.add_in != nullptr;  // only with kNorm / kFp8Block (the reduce-scatter Add codes)
     switch (ep) {
     case Epilogue::kAllReduce:
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kAllReduce, false, PAIRED>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kAllReduce, false, PAIRED, EARLY>, g, b, 0, s, pdl, a);
     case Epilogue::kNorm:
         if (add)
-            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, true, PAIRED>, g, b, 0, s, pdl, a);
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, false, PAIRED>, g, b, 0, s, pdl, a);
+            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, true, PAIRED, EARLY>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, false, PAIRED, EARLY>, g, b, 0, s, pdl, a);
     case Epilogue::kFp8Tensor:
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Tensor, false, PAIRED>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Tensor, false, PAIRED, EARLY>, g, b, 0, s, pdl, a);
     case Epilogue::kFp4:
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp4, false, PAIRED>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp4, false, PAIRED, EARLY>, g, b, 0, s, pdl, a);
     case Epilogue::kFp8Block:
         if (add)
-            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, true, PAIRED>, g, b, 0, s, pdl, a);
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, false, PAIRED>, g, b, 0, s, pdl, a);
+            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, true, PAIRED, EARLY>, g, b, 0, s, pdl,
+                                 a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, false, PAIRED, EARLY>, g, b, 0, s, pdl, a);
     }
     return cudaErrorInvalidValue;
 }
@@ -404,6 +439,17 @@ cudaError_t launch_rb(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t s)
             // 42.6) and gains from 14.  Hence from 3.5 R waves on, for R > 1.
             if (a.R == 1 || 2 * a.T >= 7 * (int64_t)a.R * wave)
                 b.prefetch_rows = wave;
+        }
+    }
+    // TS_FLAG_PDL_EARLY_READ has its own instances where it was measured to
+    // pay: 5 to 8 partials, one or two chunks a thread (the serialised
+    // per-rank reduce-scatter calls, R=8 T=8192 H=7168: FP8 1x128 220.7 us
+    // against 227.6 for the eight calls, bf16 215.8 against 219.7); elsewhere
+    // the flag is accepted and changes nothing
+    if constexpr (RB == 8) {
+        if (pdl && a.early_read) {
+            if (V == 1) return launch_rb_v<RB, 1, false, true>(ep, b, nthr, grid, pdl, s);
+            if (V == 2) return launch_rb_v<RB, 2, false, true>(ep, b, nthr, grid, pdl, s);
         }
     }
     if (V == 1) return launch_rb_v<RB, 1>(ep, b, nthr, grid, pdl, s);

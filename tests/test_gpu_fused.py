@@ -619,3 +619,66 @@ def test_reducescatter_all_ranks_in_one_launch(dev, R, T, H):
             torch.cuda.synchronize()
             for k, v in one.items():
                 assert np.array_equal(host(v), host(whole[k][start:start + count])), (rs, rank, k)
+
+
+# the early-read instances (5-8 partials, one or two chunks a thread, more rows
+# than SMs), and shapes where the flag is accepted and changes nothing
+EARLY_SHAPES = [(8, 600, 7168), (5, 300, 2048), (8, 400, 4096), (4, 100, 7168), (3, 50, 16384),
+                (2, 300, 4096), (1, 1300, 1024)]
+
+
+@pytest.mark.parametrize("R,T,H", EARLY_SHAPES, ids=[f"R{r}-T{t}-H{h}" for r, t, h in EARLY_SHAPES])
+@pytest.mark.parametrize("pattern,layout", [(1, LIN), (3, SW128), (6, LIN), (7, LIN), (0, LIN)])
+def test_early_read_gives_the_same_bits(dev, pattern, layout, R, T, H):
+    """TS_FLAG_PDL_EARLY_READ (inputs read before the dependency wait): a chain
+    of launch_with_pdl calls with it on one stream gives the bits of a plain
+    call: where it has its own instances (one and two chunks a thread, the
+    padding rows of a swizzled SF buffer) and where it changes nothing (the
+    paired, four-chunk and prefetching layouts)."""
+    inp = _inputs(R, T, H, seed=pattern + R + T)
+    scale = 300.0 if pattern == 3 else None
+    P = 512 if pattern == 7 else 0
+    want = _run_gpu(dev, pattern, inp, scale, P, layout)
+    parts = inp["partials"].to(dev)
+    res = None if pattern == 0 else inp["residual"].to(dev)
+    gamma = None if pattern == 0 else inp["gamma"].to(dev)
+    sf = None if scale is None else torch.tensor([scale], dtype=torch.float32, device=dev)
+    s = torch.cuda.Stream()
+    outs = [pkg.new_outputs(pattern, T, H, dev, partial_cols=P, sf_layout=layout, with_allreduce_out=True)
+            for _ in range(3)]
+    with torch.cuda.stream(s):
+        for o in outs:
+            pkg.ts_fused_reduce_norm(pattern, parts, res, gamma, EPS, sf, sf_layout=layout, launch_with_pdl=True,
+                                     pdl_early_read=True, stream=s, **o)
+    torch.cuda.synchronize()
+    for o in outs:
+        for k, v in o.items():
+            assert np.array_equal(host(v), want[k]), k
+
+
+@pytest.mark.parametrize("rs,form", [(7, 6), (8, 1)])
+def test_reducescatter_rank_chain_with_early_read(dev, rs, form):
+    """The per-rank calls of one reduce-scatter, back to back on one stream with
+    launch_with_pdl and TS_FLAG_PDL_EARLY_READ (no call writes another's
+    inputs), equal the one launch over every rank's slice."""
+    R, T, H = 8, 3000, 7168
+    inp = _inputs(R, T, H, seed=40 + rs)
+    g = torch.Generator().manual_seed(41)
+    add = torch.randn((T, H), generator=g).to(torch.bfloat16).to(dev)
+    parts, res, gamma = inp["partials"].to(dev), inp["residual"].to(dev), inp["gamma"].to(dev)
+    whole = pkg.new_outputs(form, T, H, dev)
+    pkg.ts_reducescatter_fused_norm(rs, parts, -1, add, res, gamma, EPS, **whole)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    per = []
+    with torch.cuda.stream(s):
+        for rank in range(R):
+            start, count = pkg.rs_token_split(T, R, rank)
+            one = pkg.new_outputs(form, count, H, dev)
+            pkg.ts_reducescatter_fused_norm(rs, parts, rank, add[start:start + count], res[start:start + count],
+                                            gamma, EPS, launch_with_pdl=True, pdl_early_read=True, stream=s, **one)
+            per.append((start, count, one))
+    torch.cuda.synchronize()
+    for start, count, one in per:
+        for k, v in one.items():
+            assert np.array_equal(host(v), host(whole[k][start:start + count])), k
