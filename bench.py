@@ -766,10 +766,13 @@ def profile_case(key: str, launches: int) -> None:
 # (pattern, R, H) and T values of the per-call table: single calls with the inputs cold in L2
 SWEEP_SHAPES = ((1, 8, 7168), (6, 8, 7168), (3, 4, 5120), (1, 2, 4096))
 SWEEP_TOKENS = (1, 16, 64, 256, 1024, 4096, 16384)
+# the other entry points in the same table: all-gather pattern 2 over R=8 slices
+# of 1536 | 512 | 64 rows, and the MiniMax QK norm on R=8 shards of q 1024 | k 128
+SWEEP_OTHER = ("allgather-fp8", "qk")
 
 
 def sweep_t(reps: int = 40) -> None:
-    """Per-call time of single fused calls (launch_with_pdl) against T, with the
+    """Per-call time of single calls (launch_with_pdl) against T, with the
     inputs cold in L2: a CUDA graph of ``reps`` x (read a 256 MB buffer, call),
     minus a graph of ``reps`` reads alone.  One JSON line per (shape, T)."""
     import torch
@@ -804,6 +807,18 @@ def sweep_t(reps: int = 40) -> None:
         with torch.cuda.stream(stream):
             return min(time_launches(g.replay, 5, stream) for _ in range(3)) / reps
 
+    def report(call, nbytes, **key):
+        def both():
+            read_flush()
+            call()
+        g = graph_of(both)
+        ms = per_call_ms(g) - per_call_ms(g_flush)
+        print(json.dumps({**key, "us": ms * 1e3, "frac": nbytes / (ms * 1e-3) / 1e9 / peak,
+                          "peak_kind": peak_kind}), flush=True)
+        del g
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
     g_flush = graph_of(read_flush)
     print(json.dumps({"flush_us": per_call_ms(g_flush) * 1e3}), flush=True)
     for p, R, H in SWEEP_SHAPES:
@@ -811,20 +826,35 @@ def sweep_t(reps: int = 40) -> None:
             inp = wl.fused_inputs(wl.FusedShape(R=R, T=T, H=H), seed=0, device=dev)
             outs = pkg.new_outputs(p, T, H, dev)
             sf = torch.tensor([100.0], device=dev) if p in (2, 3, 4, 5) else None
-
-            def both():
-                read_flush()
-                pkg.ts_fused_reduce_norm(p, inp["partials"], inp["residual"], inp["gamma"], EPS, sf,
-                                         stream=stream, launch_with_pdl=True, **outs)
-
-            g = graph_of(both)
-            ms = per_call_ms(g) - per_call_ms(g_flush)
-            nb = fused_bytes(p, R, T, H)
-            print(json.dumps({"pattern": p, "R": R, "T": T, "H": H, "us": ms * 1e3,
-                              "frac": nb / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind}), flush=True)
-            del g, inp, outs
-            torch.cuda.synchronize()
-            torch.cuda.empty_cache()
+            report(lambda: pkg.ts_fused_reduce_norm(p, inp["partials"], inp["residual"], inp["gamma"],  # noqa
+                                                    EPS, sf, stream=stream, launch_with_pdl=True, **outs),
+                   fused_bytes(p, R, T, H), pattern=p, R=R, T=T, H=H)
+            del inp, outs
+    R, q, kv, rope = 8, 1536, 512, 64
+    for T in SWEEP_TOKENS:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(0)
+        full = torch.randn((T, q + kv + rope), generator=gen, device=dev).to(torch.bfloat16)
+        ins = [full[s0:s0 + c].clone() for s0, c in (pkg.rs_token_split(T, R, r) for r in range(R))]
+        xg = (torch.rand(q, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
+        yg = (torch.rand(kv, generator=gen, device=dev) + 0.5).to(torch.bfloat16)
+        e = lambda *sh, dt=torch.bfloat16: torch.empty(sh, dtype=dt, device=dev)  # noqa: E731
+        outs = dict(allgather_out=e(T, q + kv + rope), y_norm_out=e(T, kv), quant_out=e(T, q, dt=torch.uint8),
+                    scale_out=e(T, q // 128, dt=torch.float32))
+        report(lambda: pkg.ts_allgather_fused_norm(2, ins, q, kv, rope, xg, yg, EPS, EPS,  # noqa: E731
+                                                   launch_with_pdl=True, stream=stream, **outs),
+               ag_bytes(2, T, q, kv, rope), entry="allgather-fp8", R=R, T=T, hidden=q + kv + rope)
+        del full, ins, outs
+    qs = wl.QKShape(R=8, T=1, q_shard=1024, k_shard=128, v_shard=128)
+    for T in SWEEP_TOKENS:
+        qi = wl.qk_inputs(wl.QKShape(R=qs.R, T=T, q_shard=qs.q_shard, k_shard=qs.k_shard, v_shard=qs.v_shard),
+                          seed=0, device=dev)
+        qo = torch.empty((T, qs.R * qs.q_shard), dtype=torch.bfloat16, device=dev)
+        ko = torch.empty((T, qs.R * qs.k_shard), dtype=torch.bfloat16, device=dev)
+        report(lambda: pkg.ts_qk_norm_sharded(qi["shards"], qs.q_shard, qs.k_shard, qi["q_weight"],  # noqa: E731
+                                              qi["k_weight"], EPS, qo, ko, launch_with_pdl=True, stream=stream),
+               qk_bytes(qs.R, T, qs.q_shard, qs.k_shard), entry="qk", R=qs.R, T=T)
+        del qi, qo, ko
 
 
 def c_abi_call_cost():
