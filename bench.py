@@ -522,7 +522,7 @@ def _case_builders():
     def clone_if(t, i):
         return t if i == 0 else t.clone()
 
-    def fused(key, pattern, P=0, pdl=True, layout=2, R=None, T=None, H=None, early=False):
+    def fused(key, pattern, P=0, pdl=True, layout=2, R=None, T=None, H=None, early=False, indep=False):
         """One AllReduceFusionPattern on a named workload (or an R/T/H variant of
         it); FP8 per-tensor and NVFP4 scales from the workload's own norm."""
         def build(dev, stream):
@@ -549,11 +549,11 @@ def _case_builders():
                 extra = {"sf_layout": layout} if pattern in (3, 5) else {}
                 return lambda: pkg.ts_fused_reduce_norm(pattern, parts, res, gam, EPS, sf,  # noqa: E731
                                                         launch_with_pdl=pdl, pdl_early_read=early,
-                                                        stream=stream, **extra, **outs)
+                                                        pdl_independent=indep, stream=stream, **extra, **outs)
             return _copies(make), fused_bytes(pattern, shape.R, Tn, Hn, P, sf_layout=layout), 1
         return build
 
-    def rs_add(rs_pattern, all_ranks=False, concurrent=False, early=False):
+    def rs_add(rs_pattern, all_ranks=False, concurrent=False, early=False, indep=False):
         """R per-rank calls one after the other (launch_with_pdl), one call over
         every rank's slice (rank -1), or, ``concurrent``, the R per-rank calls
         on R streams forked from and joined back to ``stream`` (the ranks run
@@ -578,10 +578,14 @@ def _case_builders():
                     calls.append((rank, a_all[start:start + count], r_all[start:start + count], outs))
 
                 def call():
+                    # with indep, rank 0's call is made without the flag: it
+                    # waits for the step before, so a run of calls made with it
+                    # never spans two steps (which share buffers)
                     for rank, a_in, res, outs in calls:
                         pkg.ts_reducescatter_fused_norm(rs_pattern, parts, rank, a_in, res, inp["gamma"], EPS,
                                                         launch_with_pdl=True, pdl_early_read=early,
-                                                        stream=stream, **outs)
+                                                        pdl_independent=indep and rank > 0, stream=stream,
+                                                        **outs)
                 if not concurrent:
                     return call
                 side = [torch.cuda.Stream(device=dev) for _ in calls]
@@ -686,6 +690,10 @@ def _case_builders():
                          "before the wait)", rs_add(8, early=True)),
         "rs-add-fp8b-early": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, all 8 rank slices (8 PDL "
                               "calls, inputs read before the wait)", rs_add(7, early=True)),
+        "rs-add-indep": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, all 8 rank slices (8 PDL calls, ranks 1-7 "
+                         "waiting only before they exit)", rs_add(8, indep=True)),
+        "rs-add-fp8b-indep": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, all 8 rank slices (8 PDL "
+                              "calls, ranks 1-7 waiting only before they exit)", rs_add(7, indep=True)),
         "rs-add-fp8b-streams": ("kRSAddResidualRMSNormFP8BlockWiseQuant R=8 T=8192 H=7168, all 8 rank slices "
                                 "(8 calls on 8 streams, one CUDA graph)", rs_add(7, concurrent=True)),
         "rs-add-streams": ("kRSAddResidualRMSNorm R=8 T=8192 H=7168, all 8 rank slices (8 calls on 8 streams, "

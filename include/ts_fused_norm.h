@@ -95,7 +95,22 @@ enum {
      * it measured faster (5 to 8 partials, rows of up to 8192 columns, more
      * rows than SMs); elsewhere, and without TS_FLAG_PDL, it is accepted and
      * changes nothing.  An extension: the pages have only launch_with_pdl. */
-    TS_FLAG_PDL_EARLY_READ = 2u
+    TS_FLAG_PDL_EARLY_READ = 2u,
+    /* With TS_FLAG_PDL, for ts_fused_reduce_norm and ts_reducescatter_fused_norm
+     * only: the kernel does all of its work without waiting for the kernels
+     * before it in the stream and waits for them only before it finishes, so it
+     * still completes after them and any later work in the stream sees every
+     * result.  It may therefore run at the same time as the earlier calls of a
+     * run of calls made with this flag and as the kernel just before that run
+     * (a call made without it waits for its predecessors before it starts and
+     * so ends the run).  The caller guarantees that none of those kernels
+     * writes this call's inputs or reads or writes its outputs: for example
+     * the per-rank calls of one reduce-scatter, which read the same inputs and
+     * write disjoint outputs.  Results are identical with and without the flag.
+     * It takes effect where TS_FLAG_PDL_EARLY_READ does; elsewhere it is
+     * accepted and changes nothing.  An extension: the pages have only
+     * launch_with_pdl. */
+    TS_FLAG_PDL_INDEPENDENT = 4u
 };
 
 /* Codes identical to `AllReduceFusionPattern` (tokenspeed trtllm.py). */
@@ -204,8 +219,8 @@ typedef struct {
  *   H             hidden size: multiple of 8, <= 16384; multiple of 128 for
  *                 patterns 6, 7; multiple of 16 for patterns 3, 5.
  *   outs          host pointer to the output set (see ts_outs_t).
- *   flags         0, TS_FLAG_PDL, or TS_FLAG_PDL | TS_FLAG_PDL_EARLY_READ; other
- *                 bits: TS_ERR_UNSUPPORTED.
+ *   flags         0, TS_FLAG_PDL, or TS_FLAG_PDL with TS_FLAG_PDL_EARLY_READ or
+ *                 TS_FLAG_PDL_INDEPENDENT; other bits: TS_ERR_UNSUPPORTED.
  *   stream        cudaStream_t.
  */
 TS_API int ts_fused_reduce_norm(int pattern, const void *const *partials, int R, const void *residual,

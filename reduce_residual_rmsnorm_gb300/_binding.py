@@ -89,10 +89,12 @@ EXPORTS = ("ts_fused_reduce_norm", "ts_reducescatter_fused_norm", "ts_allgather_
 
 TS_FLAG_PDL = 1
 TS_FLAG_PDL_EARLY_READ = 2
+TS_FLAG_PDL_INDEPENDENT = 4
 
 
-def _fused_flags(launch_with_pdl: bool, pdl_early_read: bool) -> int:
-    return (TS_FLAG_PDL if launch_with_pdl else 0) | (TS_FLAG_PDL_EARLY_READ if pdl_early_read else 0)
+def _fused_flags(launch_with_pdl: bool, pdl_early_read: bool, pdl_independent: bool) -> int:
+    return ((TS_FLAG_PDL if launch_with_pdl else 0) | (TS_FLAG_PDL_EARLY_READ if pdl_early_read else 0) |
+            (TS_FLAG_PDL_INDEPENDENT if pdl_independent else 0))
 
 
 def library(path: str | None = None):
@@ -264,7 +266,7 @@ def ts_fused_reduce_norm(pattern: int, partials, residual: torch.Tensor | None =
                          quant_out: torch.Tensor | None = None,
                          scale_out: torch.Tensor | None = None,
                          sf_layout: int = SFLayout.LINEAR, launch_with_pdl: bool = False,
-                         pdl_early_read: bool = False, stream=None) -> None:
+                         pdl_early_read: bool = False, pdl_independent: bool = False, stream=None) -> None:
     """Run one AllReduceFusionPattern (see include/ts_fused_norm.h).
 
     ``partials``: R CUDA bf16 tensors [T, H] (or one [R, T, H] tensor).
@@ -275,6 +277,10 @@ def ts_fused_reduce_norm(pattern: int, partials, residual: torch.Tensor | None =
     ``pdl_early_read``: with it, read the first inputs before waiting for the
     previous kernel (TS_FLAG_PDL_EARLY_READ; only when that kernel writes none
     of this call's inputs).
+    ``pdl_independent``: with it, run without waiting for the kernels before it
+    and wait only before finishing (TS_FLAG_PDL_INDEPENDENT; only when none of
+    the kernels of the run of such calls, nor the one just before the run,
+    writes this call's inputs or touches its outputs).
     """
     ptrs, T, H, part0 = _partials(partials)
     for name, t in (("residual", residual), ("gamma", gamma), ("allreduce_out", allreduce_out),
@@ -295,7 +301,8 @@ def ts_fused_reduce_norm(pattern: int, partials, residual: torch.Tensor | None =
     arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
     _check(library().ts_fused_reduce_norm(int(pattern), arr, len(ptrs), _ptr(residual), _ptr(gamma),
                                           float(eps), _ptr(scale_factor), int(T), int(H),
-                                          ctypes.byref(outs), _fused_flags(launch_with_pdl, pdl_early_read),
+                                          ctypes.byref(outs),
+                                          _fused_flags(launch_with_pdl, pdl_early_read, pdl_independent),
                                           _stream(stream)))
 
 
@@ -318,7 +325,7 @@ def ts_reducescatter_fused_norm(rs_pattern: int, partials, rank: int, add_in: to
                                 quant_out: torch.Tensor | None = None,
                                 scale_out: torch.Tensor | None = None,
                                 sf_layout: int = SFLayout.LINEAR, launch_with_pdl: bool = False,
-                                pdl_early_read: bool = False, stream=None) -> None:
+                                pdl_early_read: bool = False, pdl_independent: bool = False, stream=None) -> None:
     """Rank ``rank``'s reduce-scatter fusion output (see include/ts_fused_norm.h).
 
     ``partials``: R CUDA bf16 tensors [T, H] holding every token; ``add_in``,
@@ -344,7 +351,8 @@ def ts_reducescatter_fused_norm(rs_pattern: int, partials, rank: int, add_in: to
     _check(library().ts_reducescatter_fused_norm(int(rs_pattern), arr, len(ptrs), int(rank), _ptr(add_in),
                                                  _ptr(residual), _ptr(gamma), float(eps), _ptr(scale_factor),
                                                  int(T), int(H), ctypes.byref(outs),
-                                                 _fused_flags(launch_with_pdl, pdl_early_read), _stream(stream)))
+                                                 _fused_flags(launch_with_pdl, pdl_early_read, pdl_independent),
+                                                 _stream(stream)))
 
 
 def ts_allgather_fused_norm(ag_pattern: int, inputs, q_lora_rank: int, kv_lora_rank: int,

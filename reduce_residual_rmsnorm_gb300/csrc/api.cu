@@ -84,7 +84,7 @@ const char *const kOutputNames[6] = {"allreduce_out", "residual_out", "norm_out"
 
 constexpr int64_t kMaxH = 16384;
 constexpr uint32_t kKnownFlags = TS_FLAG_PDL;                           // sharded and all-gather norms
-constexpr uint32_t kFusedFlags = TS_FLAG_PDL | TS_FLAG_PDL_EARLY_READ;  // fused and reduce-scatter forms
+constexpr uint32_t kFusedFlags = TS_FLAG_PDL | TS_FLAG_PDL_EARLY_READ | TS_FLAG_PDL_INDEPENDENT;  // fused, RS
 constexpr int64_t kMaxRows = 0x7FFFFFFFLL;
 
 }  // namespace
@@ -266,7 +266,7 @@ int fused_impl(int pattern, const void *const *partials, int R, const void *add_
     a.sf_rows = sf_rows;
     a.sf_cols = sf_cols;
     const bool pdl = (flags & TS_FLAG_PDL) != 0;
-    a.early_read = pdl && (flags & TS_FLAG_PDL_EARLY_READ) ? 1 : 0;
+    a.pdl_wait = !pdl ? 0 : (flags & TS_FLAG_PDL_INDEPENDENT) ? 2 : (flags & TS_FLAG_PDL_EARLY_READ) ? 1 : 0;
 
     Epilogue ep;
     switch (pattern) {

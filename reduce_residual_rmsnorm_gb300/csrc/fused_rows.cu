@@ -60,14 +60,35 @@ constexpr int load_group()
 // and every rounding is the one of the 2V-chunk layout: a row's outputs do
 // not depend on T.
 //
-// EARLY (TS_FLAG_PDL_EARLY_READ, the caller's guarantee that the previous
-// kernel in the stream writes none of this call's inputs): the first chunk
-// group's loads are issued before the dependency wait, so they overlap that
-// kernel's last CTAs; nothing is written before the wait.
-template <int RB, int V, Epilogue EP, bool ADD, bool PAIRED, bool EARLY = false>
+// WAIT, the place of the dependency wait of a launch with programmatic
+// dependent launch:
+//   kWaitFirst  before the first memory access (TS_FLAG_PDL alone);
+//   kEarlyRead  after the first chunk group's loads are issued, so that they
+//               overlap the previous kernel's last CTAs; nothing is written
+//               before the wait (TS_FLAG_PDL_EARLY_READ: the previous kernel
+//               writes none of this call's inputs);
+//   kWaitLast   just before each thread exits, after all of its work, so the
+//               whole call can run beside the previous kernel and still
+//               completes after it (TS_FLAG_PDL_INDEPENDENT: the previous
+//               kernel writes none of this call's inputs and neither reads nor
+//               writes its outputs).
+enum : int { kWaitFirst = 0, kEarlyRead = 1, kWaitLast = 2 };
+
+template <bool kOn>
+struct WaitBeforeExit {
+    __device__ ~WaitBeforeExit()
+    {
+        if constexpr (kOn)
+            pdl_wait();
+    }
+};
+
+template <int RB, int V, Epilogue EP, bool ADD, bool PAIRED, int WAIT = kWaitFirst>
 __global__ void __maxnreg__((reg_cap<RB, V>()))
     fused_rows_kernel(const __grid_constant__ FusedArgs a)
 {
+    constexpr bool EARLY = WAIT == kEarlyRead;
+    const WaitBeforeExit<WAIT == kWaitLast> wait_at_exit;
     static_assert(!PAIRED || V <= 2, "pairs of one- or two-chunk threads");
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
@@ -107,7 +128,10 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
         }
     }
 
-    pdl_wait();
+    if constexpr (WAIT == kWaitLast)
+        pdl_launch_dependents();
+    else
+        pdl_wait();
     if constexpr (EP == Epilogue::kFp4) {
         if (row >= a.T) {  // a padding row of a swizzled SF buffer: zeros only
             uint8_t *sf = static_cast<uint8_t *>(a.scale_out);
@@ -373,27 +397,27 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     }
 }
 
-template <int RB, int V, bool PAIRED = false, bool EARLY = false>
+template <int RB, int V, bool PAIRED = false, int WAIT = kWaitFirst>
 cudaError_t launch_rb_v(Epilogue ep, const FusedArgs &a, int nthr, int64_t grid, bool pdl, cudaStream_t s)
 {
     const dim3 g((unsigned)grid), b((unsigned)nthr);
     const bool add = a.add_in != nullptr;  // only with kNorm / kFp8Block (the reduce-scatter Add codes)
     switch (ep) {
     case Epilogue::kAllReduce:
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kAllReduce, false, PAIRED, EARLY>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kAllReduce, false, PAIRED, WAIT>, g, b, 0, s, pdl, a);
     case Epilogue::kNorm:
         if (add)
-            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, true, PAIRED, EARLY>, g, b, 0, s, pdl, a);
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, false, PAIRED, EARLY>, g, b, 0, s, pdl, a);
+            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, true, PAIRED, WAIT>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, false, PAIRED, WAIT>, g, b, 0, s, pdl, a);
     case Epilogue::kFp8Tensor:
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Tensor, false, PAIRED, EARLY>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Tensor, false, PAIRED, WAIT>, g, b, 0, s, pdl, a);
     case Epilogue::kFp4:
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp4, false, PAIRED, EARLY>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp4, false, PAIRED, WAIT>, g, b, 0, s, pdl, a);
     case Epilogue::kFp8Block:
         if (add)
-            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, true, PAIRED, EARLY>, g, b, 0, s, pdl,
+            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, true, PAIRED, WAIT>, g, b, 0, s, pdl,
                                  a);
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, false, PAIRED, EARLY>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, false, PAIRED, WAIT>, g, b, 0, s, pdl, a);
     }
     return cudaErrorInvalidValue;
 }
@@ -447,9 +471,13 @@ cudaError_t launch_rb(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t s)
     // against 227.6 for the eight calls, bf16 215.8 against 219.7); elsewhere
     // the flag is accepted and changes nothing
     if constexpr (RB == 8) {
-        if (pdl && a.early_read) {
-            if (V == 1) return launch_rb_v<RB, 1, false, true>(ep, b, nthr, grid, pdl, s);
-            if (V == 2) return launch_rb_v<RB, 2, false, true>(ep, b, nthr, grid, pdl, s);
+        if (pdl && a.pdl_wait == kEarlyRead) {
+            if (V == 1) return launch_rb_v<RB, 1, false, kEarlyRead>(ep, b, nthr, grid, pdl, s);
+            if (V == 2) return launch_rb_v<RB, 2, false, kEarlyRead>(ep, b, nthr, grid, pdl, s);
+        }
+        if (pdl && a.pdl_wait == kWaitLast) {
+            if (V == 1) return launch_rb_v<RB, 1, false, kWaitLast>(ep, b, nthr, grid, pdl, s);
+            if (V == 2) return launch_rb_v<RB, 2, false, kWaitLast>(ep, b, nthr, grid, pdl, s);
         }
     }
     if (V == 1) return launch_rb_v<RB, 1>(ep, b, nthr, grid, pdl, s);

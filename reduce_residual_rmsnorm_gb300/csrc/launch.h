@@ -47,7 +47,7 @@ struct FusedArgs {
     int64_t sf_rows;    // rows of the SF buffer (T, or T padded to 128 / 8)
     int64_t sf_cols;    // H/16, padded to a multiple of 4 when swizzled
     int64_t prefetch_rows;  // rows ahead whose inputs a CTA prefetches into L2 (0: none)
-    int early_read;         // read the first chunk group before the dependency wait (TS_FLAG_PDL_EARLY_READ)
+    int pdl_wait;           // where a PDL launch waits: 0 first, 1 after the first loads, 2 before exit
 };
 
 struct QKArgs {

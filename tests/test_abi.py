@@ -144,7 +144,7 @@ NEG_FUSED = [
     ("partial_cols % 8", dict(pattern=7, P=100), SHAPE),
     ("sf layout 7", dict(pattern=5, sf_layout=7), BAD_PATTERN),
     ("reserved", dict(mutate=_set("reserved", 1)), UNSUPPORTED),
-    ("unknown flag", dict(flags=4), UNSUPPORTED),
+    ("unknown flag", dict(flags=8), UNSUPPORTED),
     ("outputs overlap", dict(mutate=lambda a, o: o.update(norm_out=o["residual_out"] + 16)), ALIAS),
     ("output overlaps partial", dict(mutate=lambda a, o: o.update(norm_out=a["partials"][1])), ALIAS),
     ("allreduce_out inside partial 0", dict(pattern=0, mutate=lambda a, o: o.update(
@@ -302,13 +302,17 @@ def test_pdl_flag_accepted(lib):
 
 
 def test_early_read_flag_only_on_the_fused_forms(lib):
-    """TS_FLAG_PDL_EARLY_READ (2) belongs to the fused and reduce-scatter entry
-    points; the sharded norms reject it."""
+    """TS_FLAG_PDL_EARLY_READ (2) and TS_FLAG_PDL_INDEPENDENT (4) belong to the
+    fused and reduce-scatter entry points; the sharded norms reject them."""
     assert _fused_call(lib, T=0, flags=3)[0] == TS_OK
     assert _fused_call(lib, T=0, flags=2)[0] == TS_OK
+    assert _fused_call(lib, T=0, flags=5)[0] == TS_OK
     assert _rs_call(lib, T=0, flags=3)[0] == TS_OK
+    assert _rs_call(lib, T=0, flags=5)[0] == TS_OK
     assert _qk_call(lib, T=0, flags=3)[0] == UNSUPPORTED
     assert _rms_call(lib, T=0, flags=2)[0] == UNSUPPORTED
+    assert _qk_call(lib, T=0, flags=5)[0] == UNSUPPORTED
+    assert _fused_call(lib, T=0, flags=8)[0] == UNSUPPORTED
 
 
 # ---------------------------------------------------------------------------

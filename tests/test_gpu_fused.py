@@ -627,14 +627,17 @@ EARLY_SHAPES = [(8, 600, 7168), (5, 300, 2048), (8, 400, 4096), (4, 100, 7168), 
                 (2, 300, 4096), (1, 1300, 1024)]
 
 
+@pytest.mark.parametrize("flag", ["early", "independent"])
 @pytest.mark.parametrize("R,T,H", EARLY_SHAPES, ids=[f"R{r}-T{t}-H{h}" for r, t, h in EARLY_SHAPES])
 @pytest.mark.parametrize("pattern,layout", [(1, LIN), (3, SW128), (6, LIN), (7, LIN), (0, LIN)])
-def test_early_read_gives_the_same_bits(dev, pattern, layout, R, T, H):
-    """TS_FLAG_PDL_EARLY_READ (inputs read before the dependency wait): a chain
-    of launch_with_pdl calls with it on one stream gives the bits of a plain
-    call: where it has its own instances (one and two chunks a thread, the
-    padding rows of a swizzled SF buffer) and where it changes nothing (the
-    paired, four-chunk and prefetching layouts)."""
+def test_early_read_gives_the_same_bits(dev, pattern, layout, R, T, H, flag):
+    """TS_FLAG_PDL_EARLY_READ (inputs read before the dependency wait) and
+    TS_FLAG_PDL_INDEPENDENT (the wait just before exit): a chain of
+    launch_with_pdl calls with the flag on one stream, each on its own outputs,
+    gives the bits of a plain call: where the flag has its own instances (one
+    and two chunks a thread, the padding rows of a swizzled SF buffer) and
+    where it changes nothing (the paired, four-chunk and prefetching
+    layouts)."""
     inp = _inputs(R, T, H, seed=pattern + R + T)
     scale = 300.0 if pattern == 3 else None
     P = 512 if pattern == 7 else 0
@@ -649,18 +652,22 @@ def test_early_read_gives_the_same_bits(dev, pattern, layout, R, T, H):
     with torch.cuda.stream(s):
         for o in outs:
             pkg.ts_fused_reduce_norm(pattern, parts, res, gamma, EPS, sf, sf_layout=layout, launch_with_pdl=True,
-                                     pdl_early_read=True, stream=s, **o)
+                                     pdl_early_read=flag == "early", pdl_independent=flag == "independent",
+                                     stream=s, **o)
     torch.cuda.synchronize()
     for o in outs:
         for k, v in o.items():
             assert np.array_equal(host(v), want[k]), k
 
 
+@pytest.mark.parametrize("flag", ["early", "independent"])
 @pytest.mark.parametrize("rs,form", [(7, 6), (8, 1)])
-def test_reducescatter_rank_chain_with_early_read(dev, rs, form):
+def test_reducescatter_rank_chain_with_early_read(dev, rs, form, flag):
     """The per-rank calls of one reduce-scatter, back to back on one stream with
-    launch_with_pdl and TS_FLAG_PDL_EARLY_READ (no call writes another's
-    inputs), equal the one launch over every rank's slice."""
+    launch_with_pdl and TS_FLAG_PDL_EARLY_READ or TS_FLAG_PDL_INDEPENDENT (no
+    call writes another's inputs or touches its outputs), equal the one launch
+    over every rank's slice; and a kernel after the chain on the same stream
+    (a copy of every slice's residual_out) sees every call's results."""
     R, T, H = 8, 3000, 7168
     inp = _inputs(R, T, H, seed=40 + rs)
     g = torch.Generator().manual_seed(41)
@@ -676,9 +683,12 @@ def test_reducescatter_rank_chain_with_early_read(dev, rs, form):
             start, count = pkg.rs_token_split(T, R, rank)
             one = pkg.new_outputs(form, count, H, dev)
             pkg.ts_reducescatter_fused_norm(rs, parts, rank, add[start:start + count], res[start:start + count],
-                                            gamma, EPS, launch_with_pdl=True, pdl_early_read=True, stream=s, **one)
+                                            gamma, EPS, launch_with_pdl=True, pdl_early_read=flag == "early",
+                                            pdl_independent=flag == "independent", stream=s, **one)
             per.append((start, count, one))
+        copies = [one["residual_out"].clone() for _, _, one in per]
     torch.cuda.synchronize()
-    for start, count, one in per:
+    for (start, count, one), c in zip(per, copies):
         for k, v in one.items():
             assert np.array_equal(host(v), host(whole[k][start:start + count])), k
+        assert np.array_equal(host(c), host(whole["residual_out"][start:start + count]))
