@@ -91,10 +91,9 @@ enum {
      * per-rank calls of one reduce-scatter, or calls on buffers produced
      * earlier); the kernel still waits before it writes any output, so a
      * previous kernel that reads this call's outputs is safe either way.
-     * Results are identical with and without the flag.  It takes effect where
-     * it measured faster (5 to 8 partials, rows of up to 8192 columns, more
-     * rows than SMs); elsewhere, and without TS_FLAG_PDL, it is accepted and
-     * changes nothing.  An extension: the pages have only launch_with_pdl. */
+     * Results are identical with and without the flag.  It takes effect for 2
+     * to 8 partials, rows of up to 8192 columns and more rows than SMs;
+     * elsewhere, and without TS_FLAG_PDL, it is accepted and changes nothing.  An extension: the pages have only launch_with_pdl. */
     TS_FLAG_PDL_EARLY_READ = 2u,
     /* With TS_FLAG_PDL, for ts_fused_reduce_norm and ts_reducescatter_fused_norm
      * only: the kernel does all of its work without waiting for the kernels

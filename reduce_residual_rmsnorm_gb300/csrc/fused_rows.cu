@@ -465,12 +465,13 @@ cudaError_t launch_rb(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t s)
                 b.prefetch_rows = wave;
         }
     }
-    // TS_FLAG_PDL_EARLY_READ has its own instances where it was measured to
-    // pay: 5 to 8 partials, one or two chunks a thread (the serialised
-    // per-rank reduce-scatter calls, R=8 T=8192 H=7168: FP8 1x128 220.7 us
-    // against 227.6 for the eight calls, bf16 215.8 against 219.7); elsewhere
-    // the flag is accepted and changes nothing
-    if constexpr (RB == 8) {
+    // TS_FLAG_PDL_EARLY_READ and TS_FLAG_PDL_INDEPENDENT have their own
+    // instances for 2 to 8 partials with one or two chunks a thread (the
+    // serialised per-rank reduce-scatter calls, FP8 1x128, eight calls of 1024
+    // rows at R=8 H=7168: 227.3 us plain, 220.9 early, 188.0 independent; four
+    // of 2048 rows at R=4: 139.3, 135.9, 128.7; two of 4096 at R=2: 101.4,
+    // 93.8, 98.6 with rank 0 unflagged); elsewhere the flags change nothing
+    if constexpr (RB >= 2 && RB <= 8) {
         if (pdl && a.pdl_wait == kEarlyRead) {
             if (V == 1) return launch_rb_v<RB, 1, false, kEarlyRead>(ep, b, nthr, grid, pdl, s);
             if (V == 2) return launch_rb_v<RB, 2, false, kEarlyRead>(ep, b, nthr, grid, pdl, s);

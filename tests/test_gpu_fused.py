@@ -621,10 +621,10 @@ def test_reducescatter_all_ranks_in_one_launch(dev, R, T, H):
                 assert np.array_equal(host(v), host(whole[k][start:start + count])), (rs, rank, k)
 
 
-# the early-read instances (5-8 partials, one or two chunks a thread, more rows
-# than SMs), and shapes where the flag is accepted and changes nothing
-EARLY_SHAPES = [(8, 600, 7168), (5, 300, 2048), (8, 400, 4096), (4, 100, 7168), (3, 50, 16384),
-                (2, 300, 4096), (1, 1300, 1024)]
+# the instances of the two flags (2-8 partials, one or two chunks a thread,
+# more rows than SMs), and shapes where a flag is accepted and changes nothing
+EARLY_SHAPES = [(8, 600, 7168), (5, 300, 2048), (8, 400, 4096), (4, 400, 7168), (3, 500, 4096),
+                (2, 600, 8192), (2, 300, 4096), (4, 100, 7168), (3, 50, 16384), (1, 1300, 1024)]
 
 
 @pytest.mark.parametrize("flag", ["early", "independent"])
