@@ -28,20 +28,21 @@ namespace {
 
 constexpr int kRowsPerCta = 8;
 
-// Where gathered row t lives: rank `rank`'s slice, local row `local`
-// (T < 2^31: 32-bit arithmetic).
+// Where gathered row t lives: rank `rank`'s slice, local row `local`.  The
+// ranks' row counts come from the host (T < 2^31), and the two divisions by
+// them are multiply-highs (int_div.h).
 __device__ __forceinline__ const uint16_t *gathered_row(const AGArgs &a, int64_t t)
 {
-    const uint32_t tu = (uint32_t)t, R = (uint32_t)a.R;
-    const uint32_t base = (uint32_t)a.T / R, extra = (uint32_t)a.T % R;
+    const uint32_t tu = (uint32_t)t;
     uint32_t rank, local;
-    if (tu < extra * (base + 1)) {
-        rank = tu / (base + 1);
-        local = tu - rank * (base + 1);
+    if (tu < a.split) {
+        rank = div_by(tu, a.div_hi);
+        local = tu - rank * (a.base + 1);
     } else {
-        const uint32_t t2 = tu - extra * (base + 1);
-        rank = extra + t2 / base;
-        local = t2 - (rank - extra) * base;
+        const uint32_t t2 = tu - a.split;
+        const uint32_t k = div_by(t2, a.div_lo);
+        rank = a.extra + k;
+        local = t2 - k * a.base;
     }
     return a.inputs[rank] + (int64_t)local * a.hidden;
 }

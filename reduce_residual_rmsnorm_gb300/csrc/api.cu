@@ -526,6 +526,11 @@ extern "C" int ts_allgather_fused_norm(int ag_pattern, const void *const *inputs
         a.inputs[r] = static_cast<const uint16_t *>(inputs[r]);
     a.R = R;
     a.T = T;
+    a.base = (uint32_t)base;
+    a.extra = (uint32_t)extra;
+    a.split = (uint32_t)(extra * (base + 1));
+    a.div_hi = tsfn::div_magic((uint32_t)(base + 1));
+    a.div_lo = tsfn::div_magic(base > 0 ? (uint32_t)base : 1u);
     a.hidden = (int)hidden;
     a.q = (int)q;
     a.kv = (int)kv;

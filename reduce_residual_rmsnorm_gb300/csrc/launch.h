@@ -8,6 +8,8 @@
 
 #include <cuda_runtime.h>
 
+#include "int_div.h"
+
 namespace tsfn {
 
 constexpr int kMaxR = 16;
@@ -74,6 +76,10 @@ struct AGArgs {
     const uint16_t *inputs[kMaxR];  // rank r's token slice [count_r, hidden]
     int R;
     int64_t T;                      // gathered tokens
+    // the token split: ranks below `extra` hold base + 1 rows (gathered rows
+    // below `split` = extra * (base + 1)), the others base rows
+    uint32_t base, extra, split;
+    DivMagic div_hi, div_lo;        // division by base + 1 and by base
     int hidden, q, kv;              // row = x (q) | y (kv) | rope
     const uint16_t *x_gamma;
     const uint16_t *y_gamma;
