@@ -8,6 +8,7 @@ square root, denormals kept (the quantisers depend on them).
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import glob
 import os
 import shutil
@@ -55,6 +56,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     if not force and up_to_date():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
+    # one build at a time: processes started together (torchrun ranks, test
+    # workers) share the object files; the later ones find the library built
+    with open(os.path.join(BUILD_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and up_to_date():
+            return LIB_PATH
+        return _build_locked(verbose, extra_flags)
+
+
+def _build_locked(verbose: bool, extra_flags: list[str] | None) -> str:
     cc = nvcc()
     flags = NVCC_FLAGS + (extra_flags or [])
 
