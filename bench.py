@@ -147,7 +147,7 @@ KERNEL_SOURCES = ("ag_norm.cu", "device_util.cuh", "fused_rows.cu", "int_div.h",
 # the device sources each kernel family is built from
 KERNEL_FAMILIES = {
     "fused_rows": ("device_util.cuh", "fused_rows.cu", "launch.h", "sf_layout.cuh"),
-    "qk_norm": ("device_util.cuh", "launch.h", "qk_norm.cu"),
+    "qk_norm": ("device_util.cuh", "int_div.h", "launch.h", "qk_norm.cu"),
     "ag_norm": ("ag_norm.cu", "device_util.cuh", "int_div.h", "launch.h"),
 }
 

@@ -404,6 +404,7 @@ int sharded_norm(const char *what, const void *const *shards, int R, int64_t T, 
     for (int r = 0; r < R; ++r)
         a.shards[r] = static_cast<const uint16_t *>(shards[r]);
     a.R = R;
+    a.div_r = tsfn::div_magic((uint32_t)R);
     a.T = T;
     a.row_stride = row_stride;
     a.Q = (int)Q;

@@ -55,6 +55,7 @@ struct FusedArgs {
 struct QKArgs {
     const uint16_t *shards[kMaxR];
     int R;
+    DivMagic div_r;  // division by R (a warp's token and shard)
     int64_t T;
     int64_t row_stride;
     int Q;

@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kMaxThreads, (QC <= 4 ? 2 : 1)) qk_norm_kernel
 {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int tl = warp / a.R;
+    const int tl = (int)div_by((uint32_t)warp, a.div_r);
     const int r = warp - tl * a.R;
     const int64_t t0 = ((int64_t)blockIdx.x * tpc + tl) * TPW;
     const int qn = a.Q >> 3, kn = a.K >> 3;
