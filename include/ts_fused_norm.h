@@ -27,10 +27,11 @@
  *     host buffers the kernel itself moves the bytes across the host link
  *     (NVLink-C2C on a Grace-Blackwell node): no staging copy is needed.  A
  *     pointer to ordinary pageable host memory is outside this contract.  The
- *     library allocates nothing, keeps no state between calls and never
- *     synchronises: a call validates its arguments on the host, enqueues one
- *     kernel on `stream` (a cudaStream_t; NULL = the legacy default stream)
- *     and returns.  Arrays of pointers (`partials`, `qkv_shards`) and the
+ *     library allocates no memory and never synchronises: a call validates
+ *     its arguments on the host, enqueues one kernel on `stream` (a
+ *     cudaStream_t; NULL = the legacy default stream) and returns.  Between
+ *     calls it keeps only the calling thread's last error detail and, per
+ *     device, the SM count and occupancy figures read on the first call.  Arrays of pointers (`partials`, `qkv_shards`) and the
  *     `ts_outs_t` struct live in HOST memory and are read during the call only.
  *   - bf16 tensors are row-major and contiguous unless a leading dimension is
  *     given.  Tensor base pointers must be 16-byte aligned (128-bit vector
