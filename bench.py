@@ -660,9 +660,9 @@ def _case_builders():
         inp = wl.fused_inputs(shape, seed=0, device=dev)
         outs = pkg.new_outputs(1, 16, 4096, dev)
 
-        def call(pdl=False):
+        def call(pdl=False, early=False):
             pkg.ts_fused_reduce_norm(1, inp["partials"], inp["residual"], inp["gamma"], EPS, stream=stream,
-                                     launch_with_pdl=pdl, **outs)
+                                     launch_with_pdl=pdl, pdl_early_read=early, **outs)
         return [call], fused_bytes(1, 2, 16, 4096), 1
 
     tp = lambda pattern, R: fused("C4", pattern, R=R, T=16384, H=5120)  # noqa: E731
@@ -740,8 +740,16 @@ def measure_rows(dev, stream, peak: float, iters: int, only=None) -> dict:
                         call(pdl=True)
                 ms_pdl = time_launches(pdl_graph.replay, 20, stream) / 100
                 del pdl_graph
+                # and with TS_FLAG_PDL_EARLY_READ: no call of the chain writes another's inputs
+                early_graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(early_graph, stream=stream):
+                    for _ in range(100):
+                        call(pdl=True, early=True)
+                ms_early = time_launches(early_graph.replay, 20, stream) / 100
+                del early_graph
                 rows[label] = {"us_stream_launch": ms_stream * 1e3, "us_in_cuda_graph": ms_graph * 1e3,
-                               "us_in_cuda_graph_pdl": ms_pdl * 1e3, "bytes": nbytes}
+                               "us_in_cuda_graph_pdl": ms_pdl * 1e3,
+                               "us_in_cuda_graph_pdl_early_read": ms_early * 1e3, "bytes": nbytes}
             else:
                 ms = time_launches(calls, iters, stream, launches_per_call=per_call)
                 rows[label] = roofline_entry(nbytes, ms, peak)

@@ -93,8 +93,10 @@ enum {
      * earlier); the kernel still waits before it writes any output, so a
      * previous kernel that reads this call's outputs is safe either way.
      * Results are identical with and without the flag.  It takes effect for 2
-     * to 8 partials, rows of up to 8192 columns and more rows than SMs;
-     * elsewhere, and without TS_FLAG_PDL, it is accepted and changes nothing.  An extension: the pages have only launch_with_pdl. */
+     * to 8 partials with rows of up to 4096 columns, and with rows of up to
+     * 8192 columns when there are more rows than SMs; elsewhere, and without
+     * TS_FLAG_PDL, it is accepted and changes nothing.  An extension: the
+     * pages have only launch_with_pdl. */
     TS_FLAG_PDL_EARLY_READ = 2u,
     /* With TS_FLAG_PDL, for ts_fused_reduce_norm and ts_reducescatter_fused_norm
      * only: the kernel does all of its work without waiting for the kernels
