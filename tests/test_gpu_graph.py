@@ -162,3 +162,58 @@ def test_rank_calls_on_concurrent_streams(dev):
             for rank, start, count, outs in per:
                 for k, v in outs.items():
                     assert np.array_equal(host(v), host(whole[k][start:start + count])), (rs, rank, k)
+
+
+@pytest.mark.parametrize("flag", ["early", "independent"])
+def test_rank_chain_with_pdl_flags_in_a_graph(dev, flag):
+    """The R per-rank reduce-scatter calls back to back on one stream with
+    launch_with_pdl and TS_FLAG_PDL_EARLY_READ or TS_FLAG_PDL_INDEPENDENT
+    (rank 0 without it, so that no run of flagged calls spans two replays),
+    captured in a CUDA graph together with a kernel that reads every slice's
+    outputs after the chain: each replay gives the bits of one launch over every
+    rank's slice, and the kernel after the chain sees all of them."""
+    R, T, H = 8, 1500, 7168
+    inp = wl.fused_inputs(wl.FusedShape(R=R, T=T, H=H, p_std=0.5), seed=33)
+    g = torch.Generator().manual_seed(34)
+    add = torch.randn((T, H), generator=g).to(torch.bfloat16).to(dev)
+    parts, res, gamma = inp["partials"].to(dev), inp["residual"].to(dev), inp["gamma"].to(dev)
+    rs, form = 7, 6
+    whole = pkg.new_outputs(form, T, H, dev)
+    pkg.ts_reducescatter_fused_norm(rs, parts, -1, add, res, gamma, 1e-6, **whole)
+    torch.cuda.synchronize()
+    per = []
+    for rank in range(R):
+        start, count = pkg.rs_token_split(T, R, rank)
+        per.append((rank, start, count, pkg.new_outputs(form, count, H, dev)))
+    gathered = torch.empty((T, H), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def chain():
+        for rank, start, count, outs in per:
+            on = rank > 0
+            pkg.ts_reducescatter_fused_norm(rs, parts, rank, add[start:start + count], res[start:start + count],
+                                            gamma, 1e-6, launch_with_pdl=True,
+                                            pdl_early_read=on and flag == "early",
+                                            pdl_independent=on and flag == "independent", stream=stream, **outs)
+        for rank, start, count, outs in per:  # reads every call's codes after the chain
+            gathered[start:start + count].copy_(outs["quant_out"])
+
+    with torch.cuda.stream(stream):
+        chain()  # warm-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        chain()
+    want_codes = host(whole["quant_out"])
+    for _ in range(2):
+        for _, _, _, outs in per:
+            for v in outs.values():
+                v.view(torch.uint8).fill_(0xA5)
+        gathered.fill_(0x5A)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        for rank, start, count, outs in per:
+            for k, v in outs.items():
+                assert np.array_equal(host(v), host(whole[k][start:start + count])), (flag, rank, k)
+        assert np.array_equal(host(gathered), want_codes), flag
