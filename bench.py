@@ -790,8 +790,12 @@ SWEEP_OTHER = ("allgather-fp8", "qk")
 
 def sweep_t(reps: int = 40) -> None:
     """Per-call time of single calls (launch_with_pdl) against T, with the
-    inputs cold in L2: a CUDA graph of ``reps`` x (read a 256 MB buffer, call),
-    minus a graph of ``reps`` reads alone.  One JSON line per (shape, T)."""
+    inputs cold in L2: a CUDA graph of ``reps`` x (copy a 256 MB buffer, call),
+    minus a graph of ``reps`` copies alone.  One JSON line per (shape, T).
+    A copy rather than a read-only pass: after a long read-only kernel every
+    kernel that writes, PyTorch's own copy included, starts several
+    microseconds slower (a 69 MB copy: 22.6 us after a 256 MB copy, 30.7 us
+    after a 256 MB reduction), which would not be this library's cost."""
     import torch
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
@@ -805,10 +809,10 @@ def sweep_t(reps: int = 40) -> None:
     peak, peak_kind = read_peaks()
     stream = torch.cuda.Stream(device=dev)
     flush = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    acc = torch.zeros(1, dtype=torch.float32, device=dev)
+    flush_dst = torch.empty_like(flush)
 
-    def read_flush():
-        torch.sum(flush, dim=0, keepdim=True, out=acc)
+    def flush_l2():
+        flush_dst.copy_(flush)
 
     def graph_of(fn):
         g = torch.cuda.CUDAGraph()
@@ -826,7 +830,7 @@ def sweep_t(reps: int = 40) -> None:
 
     def report(call, nbytes, **key):
         def both():
-            read_flush()
+            flush_l2()
             call()
         g = graph_of(both)
         ms = per_call_ms(g) - per_call_ms(g_flush)
@@ -836,7 +840,7 @@ def sweep_t(reps: int = 40) -> None:
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
 
-    g_flush = graph_of(read_flush)
+    g_flush = graph_of(flush_l2)
     print(json.dumps({"flush_us": per_call_ms(g_flush) * 1e3}), flush=True)
     for p, R, H in SWEEP_SHAPES:
         for T in SWEEP_TOKENS:

@@ -163,8 +163,12 @@ __global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_norm_kernel(const __gr
 // warps' FP8 epilogue is then covered by half the warps).
 // ---------------------------------------------------------------------------
 
-template <int CPL, int PATTERN>
-__global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_seg_kernel(const __grid_constant__ AGArgs a)
+// AHEAD: each chunk's gamma requested one chunk ahead (below).  The FP8 x
+// segment of more than 4 chunks per lane then needs the registers of 3 CTAs
+// per SM; its plain instance, at 4 CTAs per SM, serves the larger calls.
+template <int CPL, int PATTERN, bool AHEAD>
+__global__ void __launch_bounds__(kRowsPerCta * 32, (AHEAD && PATTERN == 2 && CPL > 4) ? 3 : 4)
+    ag_seg_kernel(const __grid_constant__ AGArgs a)
 {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -216,10 +220,20 @@ __global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_seg_kernel(const __gri
     uint16_t *norm_out = seg ? a.y_norm_out : a.x_norm_out;
     const int64_t norm_ld = seg ? a.kv : a.q;
 
+    // With AHEAD a chunk's gamma is requested one chunk ahead, before the
+    // previous chunk's stores: loads and stores are issued in order, so a
+    // load issued in its own iteration starts a full round trip (from DRAM on
+    // a cold call) only after the previous chunk is done.
+    uint4 gnext = make_uint4(0, 0, 0, 0);
+    if (AHEAD && cb + lane >= c0 && cb + lane < cn)
+        gnext = ld_keep(gamma + (int64_t)(cb + lane - c0) * 8);
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
         const int c = cb + lane + 32 * i;
         const bool live = c >= c0 && c < cn;
+        const uint4 gcur = gnext;
+        if (AHEAD && i + 1 < CPL && c + 32 >= c0 && c + 32 < cn)
+            gnext = ld_keep(gamma + (int64_t)(c + 32 - c0) * 8);
         float nf[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e)
@@ -227,7 +241,7 @@ __global__ void __launch_bounds__(kRowsPerCta * 32, 4) ag_seg_kernel(const __gri
         if (live) {
             float f[8], g[8];
             unpack8(v[i], f);
-            unpack8(ld_keep(gamma + (int64_t)(c - c0) * 8), g);
+            unpack8(AHEAD ? gcur : ld_keep(gamma + (int64_t)(c - c0) * 8), g);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 nf[e] = __fmul_rn(__fmul_rn(f[e], sc), g[e]);
@@ -270,20 +284,30 @@ cudaError_t launch_cpl(const AGArgs &a, bool pdl, cudaStream_t s)
 }
 
 template <int CPL>
-cudaError_t launch_seg(const AGArgs &a, bool pdl, cudaStream_t s)
+cudaError_t launch_seg(const AGArgs &a, bool pdl, cudaStream_t s, int sms)
 {
     constexpr int rows = kRowsPerCta / 2;
     const dim3 g((unsigned)((a.T + rows - 1) / rows)), b(kRowsPerCta * 32);
     switch (a.pattern) {
-    case 0: return launch_kernel(ag_seg_kernel<CPL, 0>, g, b, 0, s, pdl, a);
-    case 1: return launch_kernel(ag_seg_kernel<CPL, 1>, g, b, 0, s, pdl, a);
+    case 0: return launch_kernel(ag_seg_kernel<CPL, 0, true>, g, b, 0, s, pdl, a);
+    case 1: return launch_kernel(ag_seg_kernel<CPL, 1, true>, g, b, 0, s, pdl, a);
     default:
         // an FP8 x segment of more than 6 chunks per lane does not fit the
         // register budget without spilling: one warp per row there
-        if constexpr (CPL > 6)
+        if constexpr (CPL > 6) {
             return launch_cpl<CPL>(a, pdl, s);
-        else
-            return launch_kernel(ag_seg_kernel<CPL, 2>, g, b, 0, s, pdl, a);
+        } else if constexpr (CPL > 4) {
+            // The gammas requested ahead need 3 CTAs per SM.  Measured on R=8
+            // 1536 | 512 | 64, back-to-back launches: up to 6 rows per SM that
+            // instance is faster (T=16 3.60 us against 4.24, T=896 4.07 against
+            // 4.70); from 1024 rows on it lost at some T (5.21 against 4.68 at
+            // T=1024), so larger calls keep the plain instance.
+            if (a.T > 6 * (int64_t)sms)
+                return launch_kernel(ag_seg_kernel<CPL, 2, false>, g, b, 0, s, pdl, a);
+            return launch_kernel(ag_seg_kernel<CPL, 2, true>, g, b, 0, s, pdl, a);
+        } else {
+            return launch_kernel(ag_seg_kernel<CPL, 2, true>, g, b, 0, s, pdl, a);
+        }
     }
 }
 
@@ -299,11 +323,11 @@ cudaError_t launch_ag(const AGArgs &a, bool pdl, cudaStream_t stream)
         const int qc = a.q / 8, nch = a.hidden / 8;
         const int qpl = (qc + 31) / 32, ypl = (nch + 31) / 32 - qc / 32;
         const int seg_lane = qpl > ypl ? qpl : ypl;  // chunk slots per lane of the wider segment
-        if (seg_lane <= 1) return launch_seg<1>(a, pdl, stream);
-        if (seg_lane <= 2) return launch_seg<2>(a, pdl, stream);
-        if (seg_lane <= 4) return launch_seg<4>(a, pdl, stream);
-        if (seg_lane <= 6) return launch_seg<6>(a, pdl, stream);
-        return launch_seg<9>(a, pdl, stream);
+        if (seg_lane <= 1) return launch_seg<1>(a, pdl, stream, sms);
+        if (seg_lane <= 2) return launch_seg<2>(a, pdl, stream, sms);
+        if (seg_lane <= 4) return launch_seg<4>(a, pdl, stream, sms);
+        if (seg_lane <= 6) return launch_seg<6>(a, pdl, stream, sms);
+        return launch_seg<9>(a, pdl, stream, sms);
     }
     if (per_lane <= 1) return launch_cpl<1>(a, pdl, stream);
     if (per_lane <= 2) return launch_cpl<2>(a, pdl, stream);

@@ -69,6 +69,9 @@ CASES = [  # R, T, q, kv, rope
     (3, 7, 1408, 512, 64),     # x ends mid-warp (176 chunks); the last CTA part empty
     (5, 13, 1024, 8, 0),       # just past 4 chunks per lane
     (2, 5, 384, 1024, 8),      # x ends mid-warp, y wider than x
+    # more than 6 and at most 16 rows per SM: one warp per segment, but the
+    # wide FP8 x segment without the gammas requested ahead (4 CTAs per SM)
+    (8, 2000, 1536, 512, 64),
     # more rows than half a wave (16 per SM): the row kernel instead of one
     # warp per segment
     (8, 2600, 1536, 512, 64),
@@ -150,14 +153,16 @@ def test_full_size(dev):
 @pytest.mark.parametrize("q,kv,rope", [(1536, 512, 64), (1408, 512, 64), (384, 1024, 8), (128, 8, 0)])
 @pytest.mark.parametrize("pattern", [1, 2])
 def test_rows_do_not_depend_on_T(dev, pattern, q, kv, rope):
-    """The first 40 gathered rows in a call of their own (one warp per row
-    segment) give the same bits as in a call over 5000 rows (one warp per
-    row), also where x ends half-way through a warp."""
-    R, T, Ts = 4, 5000, 40
+    """The first 40 and 2000 gathered rows in calls of their own (one warp per
+    row segment; for 2000 rows of a wide FP8 x segment the instance without
+    the gammas requested ahead) give the same bits as in a call over 5000 rows
+    (one warp per row), also where x ends half-way through a warp."""
+    R, T = 4, 5000
     full, slices, xg, yg = _inputs(R, T, q, kv, rope, seed=q + kv + pattern)
     big = _run(dev, pattern, slices, q, kv, rope, xg, yg)
-    small_full = full[:Ts]
-    small_slices = [small_full[s0:s0 + c].clone() for s0, c in (pkg.rs_token_split(Ts, R, r) for r in range(R))]
-    small = _run(dev, pattern, small_slices, q, kv, rope, xg, yg)
-    for k, v in small.items():
-        assert np.array_equal(v, big[k][:Ts]), k
+    for Ts in (40, 2000):
+        small_full = full[:Ts]
+        small_slices = [small_full[s0:s0 + c].clone() for s0, c in (pkg.rs_token_split(Ts, R, r) for r in range(R))]
+        small = _run(dev, pattern, small_slices, q, kv, rope, xg, yg)
+        for k, v in small.items():
+            assert np.array_equal(v, big[k][:Ts]), (Ts, k)

@@ -64,12 +64,21 @@ def test_fused_row_kernel_register_tiers(resources):
 
 
 def test_allgather_norm_kernel_fits_four_ctas_per_sm(resources):
-    checked = 0
+    """Four 256-thread CTAs per SM (64 registers), except the segment form's
+    FP8 instances of more than 4 chunks per lane with the gammas requested
+    ahead, which the launcher runs only on calls of at most 6 rows per SM,
+    at three CTAs per SM (80 registers)."""
+    checked = three = 0
     for name, v in resources.items():
         if "ag_norm_kernel" in name or "ag_seg_kernel" in name:
-            assert v["regs"] <= 64, (name, v)
+            m = re.search(r"ag_seg_kernelILi(\d+)ELi2ELb1E", name)
+            if m and int(m.group(1)) > 4:
+                assert v["regs"] <= 80, (name, v)
+                three += 1
+            else:
+                assert v["regs"] <= 64, (name, v)
             checked += 1
-    assert checked >= 26
+    assert checked >= 27 and three >= 1
 
 
 def test_sharded_norm_kernels_keep_four_ctas_per_sm(resources):
