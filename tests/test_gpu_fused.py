@@ -692,3 +692,27 @@ def test_reducescatter_rank_chain_with_early_read(dev, rs, form, flag):
         for k, v in one.items():
             assert np.array_equal(host(v), host(whole[k][start:start + count])), k
         assert np.array_equal(host(c), host(whole["residual_out"][start:start + count]))
+
+
+def test_golden_sum_order(dev):
+    """The hand-derived example of tests/golden/rounding_order.txt in which the
+    order of the peers' fp32 additions decides the bf16 result: ascending from
+    a zero accumulator gives 1.0, descending would give 1.0078125.  Bit for bit
+    through the C ABI, for kAllReduce and for the allreduce_out and
+    residual_out (zero residual) of kARResidualRMSNorm."""
+    from tests.golden_util import read_fixture
+
+    c = read_fixture("rounding_order.txt")["sum_order"]
+    R, H, want = c["R"], c["H"], c["allreduce_out"][0]
+    parts = torch.tensor(np.array([np.full((1, H), b, np.uint16) for b in c["partials"]]).view(np.int16)) \
+        .view(torch.bfloat16).to(dev)
+    assert parts.shape == (R, 1, H)
+    out = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
+    pkg.ts_fused_reduce_norm(0, parts, None, None, EPS, allreduce_out=out)
+    res = torch.zeros((1, H), dtype=torch.bfloat16, device=dev)
+    gamma = torch.ones(H, dtype=torch.bfloat16, device=dev)
+    o1 = pkg.new_outputs(1, 1, H, dev, with_allreduce_out=True)
+    pkg.ts_fused_reduce_norm(1, parts, res, gamma, EPS, **o1)
+    torch.cuda.synchronize()
+    for t in (out, o1["allreduce_out"], o1["residual_out"]):
+        assert np.array_equal(host(t), np.full((1, H), want, np.uint16))

@@ -1,0 +1,67 @@
+"""Hand-derived worked examples (tests/golden/rounding_order.txt) in which the
+order of the fp32 operations decides an output bit: the peers' partials added
+in ascending order from a zero accumulator, and the norm evaluated as
+(x * scale) * weight (tokenspeed ops/communication/triton.py,
+`amd_allreduce_residual_rmsnorm_kernel`).  Each derivation is re-checked in
+exact rational arithmetic, and the other order is checked to give the other
+bit, so that the oracle's agreement pins the order itself."""
+from fractions import Fraction
+
+import numpy as np
+
+import oracle
+from tests.golden_util import bf16_bits, bf16_value, f32, f32_rsqrt, read_fixture
+
+FIX = read_fixture("rounding_order.txt")
+
+
+def test_sum_order_derivation():
+    c = FIX["sum_order"]
+    vals = [bf16_value(b) for b in c["partials"]]
+    acc = Fraction(0)
+    for v in vals:
+        acc = f32(acc + v)
+    assert bf16_bits(acc) == c["allreduce_out"][0]
+    acc = Fraction(0)
+    for v in reversed(vals):
+        acc = f32(acc + v)
+    assert bf16_bits(acc) == c["allreduce_out_if_descending"][0]
+    assert c["allreduce_out"] != c["allreduce_out_if_descending"]
+
+
+def test_sum_order_oracle():
+    c = FIX["sum_order"]
+    R, H = c["R"], c["H"]
+    parts = np.array([np.full((1, H), b, np.uint16) for b in c["partials"]])
+    assert parts.shape == (R, 1, H)
+    got = oracle.fused_reduce_norm(c["pattern"], parts)
+    assert np.array_equal(got["allreduce_out"], np.full((1, H), c["allreduce_out"][0], np.uint16))
+
+
+def _row(vals, H):
+    return np.array([vals[j % len(vals)] for j in range(H)], np.uint16)
+
+
+def test_mul_order_derivation():
+    c = FIX["mul_order"]
+    H = c["H"]
+    x = [bf16_value(b) for b in _row(c["partial"], H)]
+    g = [bf16_value(b) for b in _row(c["gamma"], H)]
+    assert all(bf16_value(b) == 0 for b in c["residual"])
+    variance = f32(sum(v * v for v in x) / H)
+    scale = f32_rsqrt(variance + c["eps"])
+    pages = [bf16_bits(f32(f32(x[j] * scale) * g[j])) for j in range(H)]
+    other = [bf16_bits(f32(x[j] * f32(scale * g[j]))) for j in range(H)]
+    assert pages == list(_row(c["norm_out"], H))
+    assert other == list(_row(c["norm_out_if_scale_times_gamma_first"], H))
+    assert pages != other
+
+
+def test_mul_order_oracle():
+    c = FIX["mul_order"]
+    H = c["H"]
+    part = _row(c["partial"], H).reshape(1, 1, H)
+    got = oracle.fused_reduce_norm(c["pattern"], part, _row(c["residual"], H).reshape(1, H),
+                                   _row(c["gamma"], H), float(c["eps"]))
+    assert np.array_equal(got["norm_out"][0], _row(c["norm_out"], H))
+    assert np.array_equal(got["residual_out"][0], _row(c["partial"], H))

@@ -52,6 +52,19 @@ MUTANTS = {
     # (an earlier rank's slice never has fewer rows, so the planted read stays in bounds)
     "ag_wrong_rank": ("const uint16_t *row = inputs[rank] + (t - start) * hidden;",
                       "const uint16_t *row = inputs[rank > 0 ? rank - 1 : 0] + (t - start) * hidden;"),
+    "fp8_tensor_divides": ("orc_e4m3_encode(n[j] * scale_factor)", "orc_e4m3_encode(n[j] / scale_factor)"),
+    "fp4_element_scale_inverted": ("float es = (d == 0.0f) ? 0.0f : g_scale / d;",
+                                   "float es = (d == 0.0f) ? 0.0f : d / g_scale;"),
+    "partial_out_one_column_short": ("if (partial && partial_norm_out && j < partial_cols)",
+                                     "if (partial && partial_norm_out && j + 1 < partial_cols)"),
+    "fp8_block_zero_scale_divides": ("quant_out[ri * H + j] = (s == 0.0f) ? 0 : orc_e4m3_encode(n[j] / s);",
+                                     "quant_out[ri * H + j] = orc_e4m3_encode(n[j] / s);"),
+    "ag_copy_drops_rope": ("for (int64_t j = 0; j < hidden; ++j)\n                allgather_out[ri * hidden + j] = row[j];",
+                           "for (int64_t j = 0; j < q + kv; ++j)\n                allgather_out[ri * hidden + j] = row[j];"),
+    "partials_descending": ("for (int r = 0; r < R; ++r)\n                acc = acc + orc_bf16_decode(partials[r][in_off + j]);",
+                            "for (int r = R - 1; r >= 0; --r)\n                acc = acc + orc_bf16_decode(partials[r][in_off + j]);"),
+    "norm_scale_times_gamma_first": ("float y = (x[j] * scale) * orc_bf16_decode(gamma[j]);",
+                                     "float y = x[j] * (scale * orc_bf16_decode(gamma[j]));"),
     "swizzle_rows_cols": ("return tile * 512 + j * 16 + i * 4 + (k % 4);",
                           "return tile * 512 + i * 16 + j * 4 + (k % 4);"),
 }
@@ -71,6 +84,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env = dict(os.environ, ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "tests/test_oracle_formats.py", "tests/test_oracle_fused.py",
-                        "tests/test_oracle_qk.py", "tests/test_oracle_rs.py", "tests/test_oracle_ag.py"], cwd=ROOT, env=env, capture_output=True,
+                        "tests/test_oracle_qk.py", "tests/test_oracle_rs.py", "tests/test_oracle_ag.py",
+                        "tests/test_oracle_golden.py"], cwd=ROOT, env=env, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 1, f"no pin caught mutant {name}:\n{r.stdout[-2000:]}"
