@@ -716,3 +716,30 @@ def test_golden_sum_order(dev):
     torch.cuda.synchronize()
     for t in (out, o1["allreduce_out"], o1["residual_out"]):
         assert np.array_equal(host(t), np.full((1, H), want, np.uint16))
+
+
+def test_golden_add_order(dev):
+    """The hand-derived reduce-scatter Add example of
+    tests/golden/rounding_order.txt: x = ((sum of partials) + add_in) +
+    residual gives bf16 1.0 where adding the residual first would give
+    1.0078125.  Bit for bit through the C ABI, for rank 0 and for the one
+    launch over every rank."""
+    from tests.golden_util import read_fixture
+
+    c = read_fixture("rounding_order.txt")["add_order"]
+    R, H = c["R"], c["H"]
+
+    def bf(vals, shape):
+        return torch.tensor(np.full(shape, vals, np.uint16).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    parts = torch.stack([bf(b, (R, H)) for b in c["partials"]])  # T = R rows, one per rank
+    gamma = bf(0x3F80, (H,))
+    for rank, rows in ((0, 1), (-1, R)):
+        outs = {k: torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+                for k in ("reducescatter_out", "residual_out", "norm_out")}
+        pkg.ts_reducescatter_fused_norm(c["pattern"], parts, rank, bf(c["add_in"][0], (rows, H)),
+                                        bf(c["residual"][0], (rows, H)), gamma, EPS, **outs)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(outs["residual_out"]), np.full((rows, H), c["residual_out"][0], np.uint16))
+        assert np.array_equal(host(outs["reducescatter_out"]),
+                              np.full((rows, H), c["reducescatter_out"][0], np.uint16))

@@ -65,3 +65,36 @@ def test_mul_order_oracle():
                                    _row(c["gamma"], H), float(c["eps"]))
     assert np.array_equal(got["norm_out"][0], _row(c["norm_out"], H))
     assert np.array_equal(got["residual_out"][0], _row(c["partial"], H))
+
+
+def _add_order_exact(parts, add_in, residual, residual_first=False):
+    s = Fraction(0)
+    for v in parts:
+        s = f32(s + v)
+    if residual_first:
+        return s, f32(f32(s + residual) + add_in)
+    return s, f32(f32(s + add_in) + residual)
+
+
+def test_add_order_derivation():
+    c = FIX["add_order"]
+    parts = [bf16_value(b) for b in c["partials"]]
+    a, r = bf16_value(c["add_in"][0]), bf16_value(c["residual"][0])
+    s, x = _add_order_exact(parts, a, r)
+    assert bf16_bits(s) == c["reducescatter_out"][0]
+    assert bf16_bits(x) == c["residual_out"][0]
+    _, y = _add_order_exact(parts, a, r, residual_first=True)
+    assert bf16_bits(y) == c["residual_out_if_residual_first"][0]
+    assert c["residual_out"] != c["residual_out_if_residual_first"]
+
+
+def test_add_order_oracle():
+    c = FIX["add_order"]
+    R, H = c["R"], c["H"]
+    parts = [np.full((R, H), b, np.uint16) for b in c["partials"]]  # T = R rows, one per rank
+    assert len(parts) == R
+    gamma = np.full(H, 0x3F80, np.uint16)
+    got = oracle.reducescatter_fused_norm(c["pattern"], parts, 0, np.full((1, H), c["add_in"][0], np.uint16),
+                                          np.full((1, H), c["residual"][0], np.uint16), gamma)
+    assert np.array_equal(got["residual_out"], np.full((1, H), c["residual_out"][0], np.uint16))
+    assert np.array_equal(got["reducescatter_out"], np.full((1, H), c["reducescatter_out"][0], np.uint16))

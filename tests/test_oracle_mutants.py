@@ -65,6 +65,16 @@ MUTANTS = {
                             "for (int r = R - 1; r >= 0; --r)\n                acc = acc + orc_bf16_decode(partials[r][in_off + j]);"),
     "norm_scale_times_gamma_first": ("float y = (x[j] * scale) * orc_bf16_decode(gamma[j]);",
                                      "float y = x[j] * (scale * orc_bf16_decode(gamma[j]));"),
+    "residual_before_add_in": (
+        "        if (add_in)\n            for (int64_t j = 0; j < H; ++j)\n"
+        "                x[j] = x[j] + orc_bf16_decode(add_in[loc_off + j]);\n\n"
+        "        /* residual add, in fp32; residual_out is its bf16 rounding */\n"
+        "        for (int64_t j = 0; j < H; ++j)\n"
+        "            x[j] = x[j] + orc_bf16_decode(residual[loc_off + j]);\n",
+        "        for (int64_t j = 0; j < H; ++j)\n"
+        "            x[j] = x[j] + orc_bf16_decode(residual[loc_off + j]);\n"
+        "        if (add_in)\n            for (int64_t j = 0; j < H; ++j)\n"
+        "                x[j] = x[j] + orc_bf16_decode(add_in[loc_off + j]);\n"),
     "swizzle_rows_cols": ("return tile * 512 + j * 16 + i * 4 + (k % 4);",
                           "return tile * 512 + i * 16 + j * 4 + (k % 4);"),
 }
