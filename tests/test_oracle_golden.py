@@ -98,3 +98,47 @@ def test_add_order_oracle():
                                           np.full((1, H), c["residual"][0], np.uint16), gamma)
     assert np.array_equal(got["residual_out"], np.full((1, H), c["residual_out"][0], np.uint16))
     assert np.array_equal(got["reducescatter_out"], np.full((1, H), c["reducescatter_out"][0], np.uint16))
+
+
+def _shard_rows(c, key, H):
+    """R shard rows of one token: shard 0 takes the first value, the others
+    the second, in every column."""
+    v0, v1 = c[key]
+    return [np.full((1, H), v0 if r == 0 else v1, np.uint16) for r in range(c["R"])]
+
+
+def _shard_exact(c, descending=False):
+    R, H = c["R"], c["H"]
+    qv = [bf16_value(c["q"][0 if r == 0 else 1]) for r in range(R)]
+    means = [f32(H * v * v / H) for v in qv]  # constant rows: the mean of squares is v^2
+    V = Fraction(0)
+    for m in (reversed(means) if descending else means):
+        V = f32(V + m)
+    scale = f32_rsqrt(f32(f32(V / R) + c["eps"]))
+    w = [bf16_value(c["wq"][0 if r == 0 else 1]) for r in range(R)]
+    return [bf16_bits(f32(f32(qv[r] * scale) * w[r])) for r in range(R)]
+
+
+def test_qk_shard_order_derivation():
+    c = FIX["qk_shard_order"]
+    want = [c["q_out"][0]] + [c["q_out"][1]] * (c["R"] - 1)
+    other = [c["q_out_if_descending"][0]] + [c["q_out_if_descending"][1]] * (c["R"] - 1)
+    assert _shard_exact(c) == want
+    assert _shard_exact(c, descending=True) == other
+    assert want != other
+
+
+def test_qk_shard_order_oracle():
+    c = FIX["qk_shard_order"]
+    R, H = c["R"], c["H"]
+    q, k = _shard_rows(c, "q", H), _shard_rows(c, "k", H)
+    shards = [np.concatenate([q[r], k[r]], axis=1) for r in range(R)]
+    wq = np.concatenate([np.full(H, c["wq"][0 if r == 0 else 1], np.uint16) for r in range(R)])
+    wk = np.concatenate([np.full(H, c["wk"][0 if r == 0 else 1], np.uint16) for r in range(R)])
+    q_out, k_out = oracle.qk_norm_sharded(shards, H, H, wq, wk, float(c["eps"]))
+    for r in range(R):
+        assert np.all(q_out[0, r * H:(r + 1) * H] == c["q_out"][0 if r == 0 else 1]), r
+        assert np.all(k_out[0, r * H:(r + 1) * H] == c["k_out"][0 if r == 0 else 1]), r
+    # the single-matrix form on the q columns alone
+    out = oracle.rms_norm_sharded(q, H, wq, float(c["eps"]))
+    assert np.array_equal(out, q_out)

@@ -75,6 +75,14 @@ MUTANTS = {
         "            x[j] = x[j] + orc_bf16_decode(residual[loc_off + j]);\n"
         "        if (add_in)\n            for (int64_t j = 0; j < H; ++j)\n"
         "                x[j] = x[j] + orc_bf16_decode(add_in[loc_off + j]);\n"),
+    "qk_shards_descending": ("for (int r = 0; r < R; ++r) {\n            const uint16_t *base = shards[r] + t * row_stride;\n"
+                             "            double sq = 0.0, sk = 0.0;",
+                             "for (int r = R - 1; r >= 0; --r) {\n            const uint16_t *base = shards[r] + t * row_stride;\n"
+                             "            double sq = 0.0, sk = 0.0;"),
+    "single_matrix_shards_descending": ("for (int r = 0; r < R; ++r) {\n            const uint16_t *base = shards[r] + t * row_stride;\n"
+                                        "            double s = 0.0;",
+                                        "for (int r = R - 1; r >= 0; --r) {\n            const uint16_t *base = shards[r] + t * row_stride;\n"
+                                        "            double s = 0.0;"),
     "swizzle_rows_cols": ("return tile * 512 + j * 16 + i * 4 + (k % 4);",
                           "return tile * 512 + i * 16 + j * 4 + (k % 4);"),
 }
