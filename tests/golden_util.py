@@ -89,3 +89,39 @@ def f32_rsqrt(t: Fraction) -> Fraction:
     a, b = f32(lo), f32(hi)
     assert a == b, "bracket too wide"
     return a
+
+
+def e4m3_code(x: Fraction) -> int:
+    """E4M3 code of ``x`` rounded to nearest, ties to even (positive normal
+    values up to 448)."""
+    r = round_bits(x, 4)
+    assert Fraction(2) ** -6 <= r <= 448
+    e = 0
+    while Fraction(2) ** e > r:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= r:
+        e += 1
+    m = (r / Fraction(2) ** e - 1) * 8
+    assert m.denominator == 1
+    return ((e + 7) << 3) | int(m)
+
+
+def e4m3_code_value(code: int) -> Fraction:
+    """Value of a positive normal E4M3 code."""
+    e, m = (code >> 3) & 0xF, code & 7
+    assert 0 < e and code < 0x7F
+    return (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+
+
+E2M1_GRID = [Fraction(v) for v in ("0", "0.5", "1", "1.5", "2", "3", "4", "6")]
+
+
+def e2m1_nibble(x: Fraction) -> int:
+    """E2M1 code (0..7) of a non-negative ``x``: the nearest grid value, ties to
+    the even code, saturating at 6."""
+    best = 0
+    for i, v in enumerate(E2M1_GRID):
+        d, db = abs(x - v), abs(x - E2M1_GRID[best])
+        if d < db or (d == db and i % 2 == 0):
+            best = i
+    return best

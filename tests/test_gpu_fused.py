@@ -743,3 +743,26 @@ def test_golden_add_order(dev):
         assert np.array_equal(host(outs["residual_out"]), np.full((rows, H), c["residual_out"][0], np.uint16))
         assert np.array_equal(host(outs["reducescatter_out"]),
                               np.full((rows, H), c["reducescatter_out"][0], np.uint16))
+
+
+@pytest.mark.parametrize("name", ["fp4_sf_order", "fp4_element_order"])
+def test_golden_fp4_order(dev, name):
+    """The hand-derived NVFP4 examples of tests/golden/rounding_order.txt, in
+    which the order of the scale products decides an E4M3 scale factor (g *
+    (amax / 6)) or an E2M1 code (n * (g / value(SF))): bit for bit through the
+    C ABI (the row's mean of squares is exactly 1, so the norm is the row)."""
+    from tests.golden_util import read_fixture
+
+    c = read_fixture("rounding_order.txt")[name]
+    H = c["H"]
+    row = np.array(c["row"], np.uint16)
+    g = float(np.array(c["scale_factor_bits"], np.uint32).view(np.float32)[0])
+    part = torch.tensor(row.reshape(1, 1, H).view(np.int16)).view(torch.bfloat16).to(dev)
+    res = torch.zeros((1, H), dtype=torch.bfloat16, device=dev)
+    gamma = torch.ones(H, dtype=torch.bfloat16, device=dev)
+    outs = pkg.new_outputs(3, 1, H, dev)
+    pkg.ts_fused_reduce_norm(3, part, res, gamma, float(c["eps"]), torch.tensor([g], device=dev), **outs)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(outs["residual_out"])[0], row)
+    assert int(host(outs["scale_out"])[0, 0]) == c["sf_block0"][0]
+    assert list(host(outs["quant_out"])[0, :8]) == c["quant_block0"]

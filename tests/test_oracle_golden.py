@@ -10,7 +10,8 @@ from fractions import Fraction
 import numpy as np
 
 import oracle
-from tests.golden_util import bf16_bits, bf16_value, f32, f32_rsqrt, read_fixture
+from tests.golden_util import (bf16_bits, bf16_value, e2m1_nibble, e4m3_code, e4m3_code_value, f32, f32_rsqrt,
+                               read_fixture)
 
 FIX = read_fixture("rounding_order.txt")
 
@@ -142,3 +143,46 @@ def test_qk_shard_order_oracle():
     # the single-matrix form on the q columns alone
     out = oracle.rms_norm_sharded(q, H, wq, float(c["eps"]))
     assert np.array_equal(out, q_out)
+
+
+def fp4_case(name):
+    """The fixture's NVFP4 case: (section, exact row values, exact g).  The
+    row's squares sum to H, so its norm (scale 1, gamma 1) is the row."""
+    c = FIX[name]
+    n = [bf16_value(b) for b in c["row"]]
+    assert len(n) == c["H"] and sum(v * v for v in n) == c["H"]
+    g = Fraction(float(np.array(c["scale_factor_bits"], np.uint32).view(np.float32)[0]))
+    return c, n, g
+
+
+def fp4_block0(n, g, g_times_amax_first=False, n_times_g_first=False):
+    """SF code and packed code bytes of the first 16-value block, each product
+    rounded to fp32 in the stated order."""
+    amax = max(abs(v) for v in n[:16])
+    s = f32(f32(g * amax) / 6) if g_times_amax_first else f32(g * f32(amax / 6))
+    sf = e4m3_code(s)
+    d = e4m3_code_value(sf)
+    es = f32(g / d)
+    nib = [e2m1_nibble(f32(f32(v * g) / d) if n_times_g_first else f32(v * es)) for v in n[:16]]
+    return sf, [nib[2 * k] | (nib[2 * k + 1] << 4) for k in range(8)]
+
+
+def test_fp4_order_derivations():
+    c, n, g = fp4_case("fp4_sf_order")
+    assert fp4_block0(n, g) == (c["sf_block0"][0], c["quant_block0"])
+    assert fp4_block0(n, g, g_times_amax_first=True)[0] == c["sf_block0_if_g_times_amax_first"][0]
+    c, n, g = fp4_case("fp4_element_order")
+    assert fp4_block0(n, g) == (c["sf_block0"][0], c["quant_block0"])
+    assert fp4_block0(n, g, n_times_g_first=True)[1] == c["quant_block0_if_n_times_g_first"]
+
+
+def test_fp4_order_oracle():
+    for name in ("fp4_sf_order", "fp4_element_order"):
+        c, n, g = fp4_case(name)
+        H = c["H"]
+        part = np.array(c["row"], np.uint16).reshape(1, 1, H)
+        got = oracle.fused_reduce_norm(c["pattern"], part, np.zeros((1, H), np.uint16),
+                                       np.full(H, 0x3F80, np.uint16), float(c["eps"]), float(g))
+        assert np.array_equal(got["residual_out"][0], np.array(c["row"], np.uint16)), name
+        assert got["sf_out"][0, 0] == c["sf_block0"][0], name
+        assert list(got["quant_out"][0, :8]) == c["quant_block0"], name

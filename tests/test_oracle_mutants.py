@@ -83,6 +83,9 @@ MUTANTS = {
                                         "            double s = 0.0;",
                                         "for (int r = R - 1; r >= 0; --r) {\n            const uint16_t *base = shards[r] + t * row_stride;\n"
                                         "            double s = 0.0;"),
+    "sf_scale_before_divide": ("orc_e4m3_encode(g_scale * (amax / 6.0f))", "orc_e4m3_encode((g_scale * amax) / 6.0f)"),
+    "fp4_scale_folded_late": ("uint8_t lo = (d == 0.0f) ? 0 : orc_e2m1_encode(n[j] * es);",
+                              "uint8_t lo = (d == 0.0f) ? 0 : orc_e2m1_encode((n[j] * g_scale) / d);"),
     "swizzle_rows_cols": ("return tile * 512 + j * 16 + i * 4 + (k % 4);",
                           "return tile * 512 + i * 16 + j * 4 + (k % 4);"),
 }
