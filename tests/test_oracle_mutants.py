@@ -86,6 +86,9 @@ MUTANTS = {
     "sf_scale_before_divide": ("orc_e4m3_encode(g_scale * (amax / 6.0f))", "orc_e4m3_encode((g_scale * amax) / 6.0f)"),
     "fp4_scale_folded_late": ("uint8_t lo = (d == 0.0f) ? 0 : orc_e2m1_encode(n[j] * es);",
                               "uint8_t lo = (d == 0.0f) ? 0 : orc_e2m1_encode((n[j] * g_scale) / d);"),
+    "fp8_block_reciprocal_multiply": ("(s == 0.0f) ? 0 : orc_e4m3_encode(n[j] / s);",
+                                      "(s == 0.0f) ? 0 : orc_e4m3_encode(n[j] * (1.0f / s));"),
+    "fp8_block_scale_reciprocal": ("float s = amax / 448.0f;", "float s = amax * (1.0f / 448.0f);"),
     "swizzle_rows_cols": ("return tile * 512 + j * 16 + i * 4 + (k % 4);",
                           "return tile * 512 + i * 16 + j * 4 + (k % 4);"),
 }
