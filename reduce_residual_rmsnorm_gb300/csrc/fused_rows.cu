@@ -83,7 +83,7 @@ struct WaitBeforeExit {
     }
 };
 
-template <int RB, int V, Epilogue EP, bool ADD, bool PAIRED, int WAIT = kWaitFirst>
+template <int RB, int V, Epilogue EP, bool ADD, bool PAIRED, int WAIT = kWaitFirst, bool GF = false>
 __global__ void __maxnreg__((reg_cap<RB, V>()))
     fused_rows_kernel(const __grid_constant__ FusedArgs a)
 {
@@ -167,15 +167,15 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     const int64_t rbase = row * a.H;
     float x[V][8];
     float ss = 0.0f;
-    // Paired one-chunk threads (calls of at most one wave of rows) request
-    // their gamma chunk with the row's loads, so that it does not wait behind
-    // the row reduction: same box, same run, R=8 H=7168 T=16, back to back
-    // 2.47 us against 2.62, single cold calls 2.76 against 3.00, and 1.60
-    // against 1.85 with the inputs in L2 and gamma in DRAM (the usual state
-    // right after the producing GEMM).  Unpaired one-chunk instances keep the
-    // load after the reduction: moved there too, R=2 H=4096 T=16384 measured
-    // 97.1 us against 94.4.
-    constexpr bool kGammaFirst = PAIRED && V == 1 && EP != Epilogue::kAllReduce;
+    // One-chunk threads in calls of at most one wave of rows (paired, or GF)
+    // request their gamma chunk with the row's loads, so that it does not
+    // wait behind the row reduction: same box, same run, R=8 H=7168 T=16,
+    // back to back 2.47 us against 2.62, single cold calls 2.76 against 3.00,
+    // and 1.60 against 1.85 with the inputs in L2 and gamma in DRAM (the
+    // usual state right after the producing GEMM).  Longer calls keep the
+    // load after the reduction: R=2 H=4096 T=16384 measured 97.1 us against
+    // 94.4 with it moved.
+    constexpr bool kGammaFirst = (PAIRED || GF) && V == 1 && EP != Epilogue::kAllReduce;
     uint4 gfirst = make_uint4(0, 0, 0, 0);
     if constexpr (kGammaFirst) {
         if (cbase < nc)
@@ -413,27 +413,27 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     }
 }
 
-template <int RB, int V, bool PAIRED = false, int WAIT = kWaitFirst>
+template <int RB, int V, bool PAIRED = false, int WAIT = kWaitFirst, bool GF = false>
 cudaError_t launch_rb_v(Epilogue ep, const FusedArgs &a, int nthr, int64_t grid, bool pdl, cudaStream_t s)
 {
     const dim3 g((unsigned)grid), b((unsigned)nthr);
     const bool add = a.add_in != nullptr;  // only with kNorm / kFp8Block (the reduce-scatter Add codes)
     switch (ep) {
     case Epilogue::kAllReduce:
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kAllReduce, false, PAIRED, WAIT>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kAllReduce, false, PAIRED, WAIT, GF>, g, b, 0, s, pdl, a);
     case Epilogue::kNorm:
         if (add)
-            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, true, PAIRED, WAIT>, g, b, 0, s, pdl, a);
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, false, PAIRED, WAIT>, g, b, 0, s, pdl, a);
+            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, true, PAIRED, WAIT, GF>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kNorm, false, PAIRED, WAIT, GF>, g, b, 0, s, pdl, a);
     case Epilogue::kFp8Tensor:
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Tensor, false, PAIRED, WAIT>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Tensor, false, PAIRED, WAIT, GF>, g, b, 0, s, pdl, a);
     case Epilogue::kFp4:
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp4, false, PAIRED, WAIT>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp4, false, PAIRED, WAIT, GF>, g, b, 0, s, pdl, a);
     case Epilogue::kFp8Block:
         if (add)
-            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, true, PAIRED, WAIT>, g, b, 0, s, pdl,
+            return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, true, PAIRED, WAIT, GF>, g, b, 0, s, pdl,
                                  a);
-        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, false, PAIRED, WAIT>, g, b, 0, s, pdl, a);
+        return launch_kernel(fused_rows_kernel<RB, V, Epilogue::kFp8Block, false, PAIRED, WAIT, GF>, g, b, 0, s, pdl, a);
     }
     return cudaErrorInvalidValue;
 }
@@ -497,7 +497,11 @@ cudaError_t launch_rb(Epilogue ep, const FusedArgs &a, bool pdl, cudaStream_t s)
             if (V == 2) return launch_rb_v<RB, 2, false, kWaitLast>(ep, b, nthr, grid, pdl, s);
         }
     }
-    if (V == 1) return launch_rb_v<RB, 1>(ep, b, nthr, grid, pdl, s);
+    if (V == 1) {
+        if (sms > 0 && grid <= sms)  // gamma with the row's loads (GF)
+            return launch_rb_v<RB, 1, false, kWaitFirst, true>(ep, b, nthr, grid, pdl, s);
+        return launch_rb_v<RB, 1>(ep, b, nthr, grid, pdl, s);
+    }
     if (V == 2) return launch_rb_v<RB, 2>(ep, b, nthr, grid, pdl, s);
     return launch_rb_v<RB, 4>(ep, b, nthr, grid, pdl, s);
 }
