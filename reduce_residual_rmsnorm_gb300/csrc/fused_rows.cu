@@ -251,8 +251,10 @@ __global__ void __maxnreg__((reg_cap<RB, V>()))
     // before the row reduction: in phase 2 chunk v+1's load would otherwise
     // issue only after chunk v's stores, one dependent L2 round trip per chunk
     // (R=8 T=16 H=7168: 2.59 us per call against 2.85; R=8 T=4096 H=7168:
-    // 90.5 us against 91.2).  With one chunk there is nothing to overlap and
-    // the early load measured slower (R=2 T=16 H=4096: 1.82 us against 1.78).
+    // 90.5 us against 91.2).  With one chunk there is no chain to break: a
+    // load here, after the row's loads have returned, measured slower (R=2
+    // T=16 H=4096: 1.82 us against 1.78), and short calls take the load with
+    // the row's loads instead (kGammaFirst above).
     constexpr bool kEarlyGamma = V >= 2 && EP != Epilogue::kAllReduce;
     uint4 gv[V];
     if constexpr (kEarlyGamma) {
